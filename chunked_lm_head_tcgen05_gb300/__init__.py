@@ -1,0 +1,258 @@
+"""Chunked LM-head log-prob + entropy head for GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/lmhead.h`` (``liblmhead.so``,
+built by ``buildlib.py``).  The functions named ``lmhead_*`` mirror the C entry
+points one to one and only marshal arguments: torch tensors supply device
+memory and the CUDA stream, every step of the computation runs in the
+library's kernels.  There is no CPU or PyTorch fallback: if the library is
+missing or cannot load, every call raises.
+
+``forward`` / ``backward`` are conveniences that allocate the outputs and the
+workspace with torch and raise ``LmheadError`` on a non-zero status.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "LmheadError", "library", "library_path", "build",
+    "LMHEAD_OP_FWD", "LMHEAD_OP_BWD", "STATUS_NAMES",
+    "lmhead_workspace_size", "lmhead_logps_fwd", "lmhead_logps_bwd",
+    "lmhead_read_device_status", "lmhead_read_scored_count", "lmhead_status_string",
+    "lmhead_plan_info", "lmhead_profile_enable", "lmhead_profile_count",
+    "lmhead_profile_record", "lmhead_launch_count", "forward", "backward",
+]
+
+LMHEAD_OP_FWD = 0
+LMHEAD_OP_BWD = 1
+STATUS_NAMES = {
+    0: "LMHEAD_OK", 1: "LMHEAD_ERR_INVALID_ARG", 2: "LMHEAD_ERR_UNSUPPORTED",
+    3: "LMHEAD_ERR_WORKSPACE_TOO_SMALL", 4: "LMHEAD_ERR_CUDA",
+    5: "LMHEAD_ERR_DEVICE_TIMEOUT", 6: "LMHEAD_ERR_BAD_TARGET",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "liblmhead.so")
+_lib = None
+
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes), exactly the declarations of include/lmhead.h
+_SIGNATURES = {
+    "lmhead_workspace_size": (_SZ, [ctypes.c_int, _I64, _I32, _I32, _I32]),
+    "lmhead_logps_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, ctypes.c_float,
+                                        _I32, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "lmhead_logps_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, ctypes.c_float,
+                                        _I32, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, _VP,
+                                        _SZ, _VP]),
+    "lmhead_read_device_status": (ctypes.c_int, [_VP, _VP]),
+    "lmhead_read_scored_count": (_I64, [_VP, _VP]),
+    "lmhead_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "lmhead_plan_info": (ctypes.c_int, [_I64, _I32, _I32, _I32, ctypes.POINTER(_I32),
+                                        ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "lmhead_profile_enable": (None, [ctypes.c_int]),
+    "lmhead_profile_count": (ctypes.c_int, []),
+    "lmhead_profile_record": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
+                                             ctypes.POINTER(ctypes.c_float)]),
+    "lmhead_launch_count": (ctypes.c_uint64, []),
+}
+
+
+class LmheadError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = int(status)
+        super().__init__("%s%s" % (where + ": " if where else "",
+                                   STATUS_NAMES.get(self.status, "status %d" % self.status)))
+
+
+def build(force=False):
+    """Compile liblmhead.so for sm_103a (nvcc); returns its path."""
+    from . import buildlib
+    return buildlib.build(force=force)
+
+
+def library():
+    """The loaded liblmhead.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError("liblmhead.so is not built (run chunked_lm_head_tcgen05_gb300.build())")
+        lib = ctypes.CDLL(library_path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensor(t, name, dtype, shape, allow_none=False):
+    import torch
+    if t is None:
+        if allow_none:
+            return
+        raise ValueError("%s is required" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    del torch
+
+
+def lmhead_workspace_size(op, T, H, V, chunk_size):
+    return int(library().lmhead_workspace_size(op, T, H, V, chunk_size))
+
+
+def lmhead_logps_fwd(hidden, weight, targets, loss_mask, temperature, chunk_size, logp, entropy,
+                     lse, workspace, stream=None):
+    """C ``lmhead_logps_fwd`` on torch tensors; returns the status code."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight, "weight", torch.bfloat16, (V, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(logp, "logp", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    return int(library().lmhead_logps_fwd(
+        _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
+        int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
+                     grad_entropy, lse, entropy, d_hidden, d_weight, accumulate_dweight, workspace,
+                     stream=None):
+    """C ``lmhead_logps_bwd`` on torch tensors; returns the status code."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight, "weight", torch.bfloat16, (V, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(grad_logp, "grad_logp", torch.float32, (T,), allow_none=True)
+    _check_tensor(grad_entropy, "grad_entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(d_hidden, "d_hidden", torch.float32, (T, H))
+    _check_tensor(d_weight, "d_weight", torch.float32, (V, H))
+    return int(library().lmhead_logps_bwd(
+        _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
+        int(chunk_size), _ptr(grad_logp), _ptr(grad_entropy), _ptr(lse), _ptr(entropy),
+        _ptr(d_hidden), _ptr(d_weight), int(bool(accumulate_dweight)), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lmhead_read_device_status(workspace, stream=None):
+    return int(library().lmhead_read_device_status(_ptr(workspace), _stream(stream)))
+
+
+def lmhead_read_scored_count(workspace, stream=None):
+    return int(library().lmhead_read_scored_count(_ptr(workspace), _stream(stream)))
+
+
+def lmhead_status_string(status):
+    return library().lmhead_status_string(int(status)).decode()
+
+
+def lmhead_plan_info(T, H, V, chunk_size):
+    """(fwd_splits, bwd_tokens, bwd_vocab) for these sizes on the current device."""
+    a, b, c = _I32(), _I32(), _I32()
+    rc = library().lmhead_plan_info(T, H, V, chunk_size, ctypes.byref(a), ctypes.byref(b),
+                                    ctypes.byref(c))
+    if rc:
+        raise LmheadError(rc, "lmhead_plan_info")
+    return a.value, b.value, c.value
+
+
+def lmhead_profile_enable(on):
+    library().lmhead_profile_enable(int(bool(on)))
+
+
+def lmhead_profile_count():
+    return int(library().lmhead_profile_count())
+
+
+def lmhead_profile_record(i):
+    """(kernel name, milliseconds) of the i-th recorded launch."""
+    name = ctypes.c_char_p()
+    ms = ctypes.c_float()
+    rc = library().lmhead_profile_record(i, ctypes.byref(name), ctypes.byref(ms))
+    if rc:
+        raise LmheadError(rc, "lmhead_profile_record")
+    return name.value.decode(), float(ms.value)
+
+
+def lmhead_launch_count():
+    return int(library().lmhead_launch_count())
+
+
+# ----------------------------------------------------------------- conveniences
+def _workspace(op, T, H, V, chunk_size, device):
+    import torch
+    n = lmhead_workspace_size(op, T, H, V, chunk_size)
+    if n == 0:
+        raise LmheadError(1, "lmhead_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def forward(hidden, weight, targets, loss_mask=None, temperature=1.0, chunk_size=512,
+            with_entropy=True, workspace=None, stream=None):
+    """Returns (logp, entropy or None, lse) as fp32 CUDA tensors."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev) if with_entropy else None
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _workspace(LMHEAD_OP_FWD, T, H, V, chunk_size, dev)
+    rc = lmhead_logps_fwd(hidden, weight, targets, loss_mask, temperature, chunk_size, logp, ent,
+                          lse, workspace, stream)
+    if rc:
+        raise LmheadError(rc, "lmhead_logps_fwd")
+    return logp, ent, lse
+
+
+def backward(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
+             grad_entropy, lse, entropy=None, d_weight=None, accumulate_dweight=False,
+             workspace=None, stream=None):
+    """Returns (d_hidden [T,H] fp32, d_weight [V,H] fp32)."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    d_hidden = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if d_weight is None:
+        d_weight = torch.empty((V, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = _workspace(LMHEAD_OP_BWD, T, H, V, chunk_size, dev)
+    rc = lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
+                          grad_entropy, lse, entropy, d_hidden, d_weight, accumulate_dweight,
+                          workspace, stream)
+    if rc:
+        raise LmheadError(rc, "lmhead_logps_bwd")
+    return d_hidden, d_weight

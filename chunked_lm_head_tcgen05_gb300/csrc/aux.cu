@@ -1,0 +1,238 @@
+// Memory-bound helper kernels around the tensor-core GEMMs: mask
+// compaction and target wrap, the gather of scored hidden rows, the
+// log-sum-exp combine of per-split statistics, the per-row backward
+// coefficients and the zeroing of unscored rows.
+#include "kernels.h"
+
+#include <cmath>
+
+namespace lmh {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kCompactThreads = 1024;
+
+// Wrap of negative ids (y in [-V, 0) -> y + V); -1 when the id is invalid.
+__device__ __forceinline__ int wrap_target(int y, int V) {
+  if (y < 0) y += V;
+  return (y >= 0 && y < V) ? y : -1;
+}
+
+__global__ void clear_state_kernel(DeviceState* st, int rows) {
+  st->status = 0;
+  st->rows = rows;
+}
+
+// One CTA: stable compaction of the scored positions (ascending order), the
+// wrapped targets in compact order, and the scored count.
+__global__ void __launch_bounds__(kCompactThreads)
+    compact_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ targets, int T,
+                   int V, int T_alloc, int* __restrict__ idx, int* __restrict__ y_c,
+                   DeviceState* st) {
+  __shared__ int warp_tot[kCompactThreads / 32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, w = tid >> 5;
+  const int seg = (T + kCompactThreads - 1) / kCompactThreads;
+  const int b = min(T, tid * seg);
+  const int e = min(T, b + seg);
+  int cnt = 0;
+  for (int t = b; t < e; ++t) cnt += mask[t] != 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int s = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += x;
+    }
+    warp_tot[lane] = s;   // inclusive prefix over warps
+  }
+  __syncthreads();
+  int pos = incl - cnt + (w > 0 ? warp_tot[w - 1] : 0);
+  const int total = warp_tot[kCompactThreads / 32 - 1];
+  int bad = 0;
+  for (int t = b; t < e; ++t) {
+    if (mask[t]) {
+      const int y = wrap_target(targets[t], V);
+      bad |= (y < 0);
+      idx[pos] = t;
+      y_c[pos] = y;
+      ++pos;
+    }
+  }
+  for (int r = total + tid; r < T_alloc; r += kCompactThreads) y_c[r] = -1;
+  if (bad) atomicCAS(&st->status, 0, STATUS_BAD_TARGET);
+  if (tid == 0) st->rows = total;
+}
+
+__global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T, int V, int T_alloc,
+                                     int* __restrict__ y_c, DeviceState* st) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= T_alloc) return;
+  int y = -1;
+  if (r < T) {
+    y = wrap_target(targets[r], V);
+    if (y < 0) atomicCAS(&st->status, 0, STATUS_BAD_TARGET);
+  }
+  y_c[r] = y;
+}
+
+// h_c[r] = hidden[idx[r]] for scored rows; zero rows up to T_alloc so that
+// every tile edge past the scored count reads exact zeros.
+__global__ void gather_rows_kernel(const uint4* __restrict__ hidden, int H8, const int* __restrict__ idx,
+                                   int T_alloc, const DeviceState* st, uint4* __restrict__ h_c) {
+  const int rows = st->rows;
+  const int64_t n = static_cast<int64_t>(T_alloc) * H8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / H8);
+    const int c = static_cast<int>(i - static_cast<int64_t>(r) * H8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < rows) v = hidden[static_cast<int64_t>(idx[r]) * H8 + c];
+    h_c[i] = v;
+  }
+}
+
+__global__ void zero_masked_outputs_kernel(const uint8_t* __restrict__ mask, int T, float* logp,
+                                           float* entropy, float* lse) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T || mask[t]) return;
+  logp[t] = 0.f;
+  lse[t] = 0.f;
+  if (entropy) entropy[t] = 0.f;
+}
+
+// Combine the per-split statistics (m_j, s_j, S1_j, zy_j), all in log2
+// units, by their log-sum-exp and write the token's outputs in original
+// order.  Splits are combined in a fixed order, so the result is
+// deterministic.
+__global__ void fwd_merge_kernel(const float4* __restrict__ part, int n_splits, int part_ld,
+                                 const int* __restrict__ idx, const int* __restrict__ y_c,
+                                 const DeviceState* st, float* logp, float* entropy, float* lse) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= st->rows) return;
+  float M = -INFINITY;
+  for (int j = 0; j < n_splits; ++j) M = fmaxf(M, part[static_cast<int64_t>(j) * part_ld + r].x);
+  float s = 0.f, s1 = 0.f, zy = -INFINITY;
+  for (int j = 0; j < n_splits; ++j) {
+    const float4 q = part[static_cast<int64_t>(j) * part_ld + r];
+    const float dm = q.x - M;
+    const float wgt = exp2f(dm);
+    s = fmaf(q.y, wgt, s);
+    s1 = fmaf(wgt, fmaf(dm, q.y, q.z), s1);
+    zy = fmaxf(zy, q.w);
+  }
+  const float l2s = log2f(s);
+  const int t = idx ? idx[r] : r;
+  lse[t] = (M + l2s) * kLn2;
+  logp[t] = y_c[r] >= 0 ? (zy - M - l2s) * kLn2 : __int_as_float(0x7fc00000);
+  if (entropy) entropy[t] = kLn2 * (l2s - s1 / s);
+}
+
+// Per scored row: {lse * log2 e, g_e ln2 / tau, (g_l + g_e H) / tau, g_l / tau}
+// so that dz / tau = -p (a d + b) + c [v == y], with d = log2 p.  Rows past
+// the scored count get zeros (their dz is then exactly zero).
+__global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* st, int T_alloc,
+                                const float* __restrict__ lse, const float* __restrict__ entropy,
+                                const float* __restrict__ grad_logp,
+                                const float* __restrict__ grad_entropy, float inv_tau,
+                                float4* __restrict__ coef) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= T_alloc) return;
+  float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (r < st->rows) {
+    const int t = idx ? idx[r] : r;
+    const float gl = grad_logp ? grad_logp[t] : 0.f;
+    const float ge = grad_entropy ? grad_entropy[t] : 0.f;
+    const float Hh = (grad_entropy && entropy) ? entropy[t] : 0.f;
+    c.x = lse[t] * kLog2e;
+    c.y = ge * kLn2 * inv_tau;
+    c.z = fmaf(ge, Hh, gl) * inv_tau;
+    c.w = gl * inv_tau;
+  }
+  coef[r] = c;
+}
+
+__global__ void zero_masked_rows_kernel(const uint8_t* __restrict__ mask, int T, int H4,
+                                        float4* __restrict__ d_hidden) {
+  const int64_t n = static_cast<int64_t>(T) * H4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / H4);
+    if (!mask[t]) d_hidden[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+int grid_for(int64_t n, int threads, int cap = 4 * 152 * 8) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < cap ? g : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s) {
+  clear_state_kernel<<<1, 1, 0, s>>>(st, rows_if_dense);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
+                           int* idx, int* y_c, DeviceState* st, cudaStream_t s) {
+  compact_kernel<<<1, kCompactThreads, 0, s>>>(mask, targets, T, V, T_alloc, idx, y_c, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
+                                 DeviceState* st, cudaStream_t s) {
+  targets_dense_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(targets, T, V, T_alloc, y_c, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
+                               const DeviceState* st, uint16_t* h_c, cudaStream_t s) {
+  const int H8 = H / 8;
+  gather_rows_kernel<<<grid_for(static_cast<int64_t>(T_alloc) * H8, 256), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(hidden), H8, idx, T_alloc, st, reinterpret_cast<uint4*>(h_c));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
+                                       float* lse, cudaStream_t s) {
+  zero_masked_outputs_kernel<<<(T + 255) / 256, 256, 0, s>>>(mask, T, logp, entropy, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
+                             const int* y_c, const DeviceState* st, int T_alloc, float* logp,
+                             float* entropy, float* lse, cudaStream_t s) {
+  fwd_merge_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(partials, n_splits, part_ld, idx, y_c, st,
+                                                          logp, entropy, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int T_alloc, const float* lse,
+                            const float* entropy, const float* grad_logp,
+                            const float* grad_entropy, float tau, float4* coef, cudaStream_t s) {
+  bwd_prep_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(idx, st, T_alloc, lse, entropy, grad_logp,
+                                                         grad_entropy, 1.0f / tau, coef);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
+                                    cudaStream_t s) {
+  const int H4 = H / 4;
+  zero_masked_rows_kernel<<<grid_for(static_cast<int64_t>(T) * H4, 256), 256, 0, s>>>(
+      mask, T, H4, reinterpret_cast<float4*>(d_hidden));
+  return cudaGetLastError();
+}
+
+}  // namespace lmh

@@ -1,0 +1,103 @@
+// Internal interface between the host planner (lmhead_api.cu) and the
+// sm_103a kernels.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace lmh {
+
+// Tile shape of every tensor-core GEMM in the head: 128 rows (one TMEM lane
+// per row) x 256 columns (fp32 accumulator columns), K staged 64 bf16 = one
+// 128-byte swizzle row at a time.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr uint32_t A_TILE_BYTES = BM * BK * 2;
+constexpr uint32_t B_TILE_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int EPI_WARPS = 4;
+constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators, double buffered
+constexpr size_t GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+// Device status word values (same numbers as the public lmhead_status).
+constexpr int STATUS_DEVICE_TIMEOUT = 5;
+constexpr int STATUS_BAD_TARGET = 6;
+
+// Small block of device state at the head of the workspace.
+struct DeviceState {
+  int status;       // first error seen on the device (0 = none)
+  int rows;         // number of scored tokens T_v (written by the compaction step)
+  int pad[62];
+};
+
+enum EpiKind : int {
+  EPI_FWD_STATS = 0,   // online max / exp-sum / sum p*z / target logit per vocab split
+  EPI_BWD_DZ = 1,      // dz = g_l (onehot - p) - g_e p (log p + H), divided by tau, to bf16
+  EPI_STORE_F32 = 2,   // plain fp32 tile store or read-modify-write (dh, dW)
+};
+
+struct GemmArgs {
+  // Problem extents.  M and K can be bounded by the device count of scored
+  // tokens: extent = clamp(*dev_rows - dyn_base, 0, cap).
+  int m_cap;
+  int n_extent;
+  int k_cap;
+  int m_dynamic;
+  int k_dynamic;
+  int dyn_base;
+  const int* dev_rows;
+  int n_splits;          // EPI_FWD_STATS: vocab splits per token block; else 0
+  int* status;
+  // epilogue inputs
+  float scale;           // log2(e) / tau
+  int row_base;          // offset of row 0 in the per-row arrays
+  int col_base;          // vocabulary id of column 0 (targets are global ids)
+  const int* y_c;        // per-row wrapped target id, or -1
+  float4* partials;      // EPI_FWD_STATS: [n_splits][part_ld] {m, s, S1, zy} in log2 units
+  int part_ld;
+  const float4* coef;    // EPI_BWD_DZ: per row {lse*log2e, g_e ln2/tau, (g_l + g_e H)/tau, g_l/tau}
+  uint16_t* dz_out;      // EPI_BWD_DZ: bf16 scratch, row-major, ld = dz_ld
+  int dz_ld;
+  float* out;            // EPI_STORE_F32: output rows
+  int64_t out_ld;
+  const int* row_map;    // EPI_STORE_F32: optional output row of row (row_base + r)
+  int accumulate;        // EPI_STORE_F32: 1 = add to the existing values
+  int zero_if_empty;     // EPI_STORE_F32: K == 0 and !accumulate writes zeros
+};
+
+// Launchers.  Each returns the launch error (cudaSuccess when enqueued).
+// A and B are described by TMA maps built on the host; a_mn / b_mn select
+// MN-major operand layouts.
+cudaError_t launch_gemm_fwd_stats(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p,
+                                  int grid, cudaStream_t s);
+cudaError_t launch_gemm_bwd_dz(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p,
+                               int grid, cudaStream_t s);
+cudaError_t launch_gemm_dh(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p, int grid,
+                           cudaStream_t s);
+cudaError_t launch_gemm_dw(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p, int grid,
+                           cudaStream_t s);
+
+// Auxiliary kernels (aux.cu).
+cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
+                           int* idx, int* y_c, DeviceState* st, cudaStream_t s);
+cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
+                                 DeviceState* st, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
+                               const DeviceState* st, uint16_t* h_c, cudaStream_t s);
+cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
+                                       float* lse, cudaStream_t s);
+cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
+                             const int* y_c, const DeviceState* st, int T_alloc, float* logp,
+                             float* entropy, float* lse, cudaStream_t s);
+cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int T_alloc, const float* lse,
+                            const float* entropy, const float* grad_logp,
+                            const float* grad_entropy, float tau, float4* coef, cudaStream_t s);
+cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
+                                    cudaStream_t s);
+cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s);
+
+}  // namespace lmh

@@ -1,0 +1,532 @@
+// Host side of the C ABI declared in include/lmhead.h: argument checks, the
+// tile/split/block plan, the workspace carve-up, TMA descriptor encoding and
+// the stream-ordered launches.  No device memory is allocated here and no
+// call synchronises the stream except the explicit status readers.
+#include "lmhead.h"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+
+using namespace lmh;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSplits = 32;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+int64_t ceil_div(int64_t x, int64_t m) { return (x + m - 1) / m; }
+
+// ------------------------------------------------------------------ launches
+std::atomic<uint64_t> g_launches{0};
+
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+template <class F>
+cudaError_t launch(const char* name, cudaStream_t s, F&& f) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) {
+      a = pooled_event();
+      b = pooled_event();
+    }
+  }
+  if (a && b) cudaEventRecord(a, s);
+  const cudaError_t e = f();
+  if (a && b) {
+    cudaEventRecord(b, s);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back({name, a, b});
+  }
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
+// ------------------------------------------------------------------ device facts
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map: `inner` contiguous elements per row, `outer` rows, rows
+// `row_bytes` apart; boxes of box_inner x box_outer with 128-byte swizzle.
+// Elements outside the map read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+  auto enc = encode_fn();
+  if (!enc || inner == 0 || outer == 0) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ plans
+// Vocabulary splits for the forward: each CTA takes (token block, split)
+// units round robin; pick the split count whose largest per-CTA tile count
+// is smallest (ties: fewer splits, i.e. fewer partial statistics).
+int choose_splits(int64_t m_tiles, int64_t n_tiles, int sms) {
+  struct Key {
+    int64_t m, n;
+    int sms, splits;
+  };
+  static std::mutex mu;
+  static std::vector<Key> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Key& k : cache)
+      if (k.m == m_tiles && k.n == n_tiles && k.sms == sms) return k.splits;
+  }
+  int best = 1;
+  int64_t best_span = INT64_MAX;
+  const int smax = static_cast<int>(std::min<int64_t>(n_tiles, kMaxSplits));
+  std::vector<int64_t> load;
+  for (int S = 1; S <= smax; ++S) {
+    const int64_t units = m_tiles * S;
+    const int64_t G = std::min<int64_t>(units, sms);
+    load.assign(static_cast<size_t>(G), 0);
+    for (int64_t u = 0; u < units; ++u) {
+      const int64_t j = u / m_tiles;
+      load[static_cast<size_t>(u % G)] += (j + 1) * n_tiles / S - j * n_tiles / S;
+    }
+    const int64_t span = *std::max_element(load.begin(), load.end());
+    if (span < best_span) {
+      best_span = span;
+      best = S;
+    }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() > 64) cache.clear();
+  cache.push_back({m_tiles, n_tiles, sms, best});
+  return best;
+}
+
+struct BwdPlan {
+  int64_t Tb, Vb, n_tb, n_vb;
+};
+
+// Backward blocks T_b x V_b with T_b * V_b <= chunk_size * V (the scratch
+// bound); T_b ~ V_b ~ sqrt(chunk_size * V) minimises the fp32
+// read-modify-write traffic of dh and dW, 8 T V H (1/T_b + 1/V_b) bytes.
+BwdPlan plan_bwd(int64_t T, int64_t V, int64_t chunk) {
+  BwdPlan p;
+  const int64_t T_alloc = round_up(T, BM);
+  const int64_t V_pad = round_up(V, BN);
+  const double S = static_cast<double>(chunk) * static_cast<double>(V);
+  int64_t tb_max = static_cast<int64_t>(std::floor(std::sqrt(S) / BM)) * BM;
+  tb_max = std::max<int64_t>(BM, std::min<int64_t>(tb_max, T_alloc));
+  p.n_tb = ceil_div(T_alloc, tb_max);
+  p.Tb = round_up(ceil_div(T_alloc, p.n_tb), BM);
+  int64_t vb_max = static_cast<int64_t>(std::floor(S / static_cast<double>(p.Tb) / BN)) * BN;
+  vb_max = std::max<int64_t>(BN, std::min<int64_t>(vb_max, V_pad));
+  p.n_vb = ceil_div(V_pad, vb_max);
+  p.Vb = round_up(ceil_div(V_pad, p.n_vb), BN);
+  p.n_vb = ceil_div(V, p.Vb);
+  return p;
+}
+
+struct Layout {
+  size_t state, idx, y_c, h_c, part, coef, dz, total;
+};
+
+Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
+  Layout L{};
+  const int64_t T_alloc = round_up(T, BM);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.state = take(sizeof(DeviceState));
+  L.idx = take(4 * static_cast<size_t>(T_alloc));
+  L.y_c = take(4 * static_cast<size_t>(T_alloc));
+  L.h_c = take(2 * static_cast<size_t>(T_alloc) * static_cast<size_t>(H));
+  if (op == LMHEAD_OP_FWD) {
+    L.part = take(16 * static_cast<size_t>(kMaxSplits) * static_cast<size_t>(T_alloc));
+  } else {
+    const BwdPlan bp = plan_bwd(T, V, chunk);
+    L.coef = take(16 * static_cast<size_t>(T_alloc));
+    L.dz = take(2 * static_cast<size_t>(bp.Tb) * static_cast<size_t>(bp.Vb));
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+lmhead_status check_sizes(int64_t T, int32_t H, int32_t V, float tau, int32_t chunk) {
+  if (T < 0 || H <= 0 || V <= 0 || chunk <= 0 || !std::isfinite(tau) || !(tau > 0.f))
+    return LMHEAD_ERR_INVALID_ARG;
+  if (H % 64 != 0 || T >= (int64_t{1} << 31) - 256) return LMHEAD_ERR_UNSUPPORTED;
+  return LMHEAD_OK;
+}
+
+#define LMH_TRY(expr)                               \
+  do {                                              \
+    if ((expr) != cudaSuccess) return LMHEAD_ERR_CUDA; \
+  } while (0)
+
+// Shared front half of both calls: status reset, mask compaction / target
+// wrap, and the gather of scored rows.  Sets the row source for the GEMMs.
+struct Front {
+  DeviceState* st;
+  int* idx;             // NULL when every token is scored
+  int* y_c;
+  const uint16_t* h_src;
+  int64_t rows_avail;   // rows addressable in h_src
+  int64_t T_alloc;
+};
+
+lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_t* mask, int64_t T,
+                    int32_t H, int32_t V, char* ws, const Layout& L, cudaStream_t s, Front* f) {
+  f->T_alloc = round_up(T, BM);
+  f->st = reinterpret_cast<DeviceState*>(ws + L.state);
+  f->y_c = reinterpret_cast<int*>(ws + L.y_c);
+  const int Ti = static_cast<int>(T), Ta = static_cast<int>(f->T_alloc);
+  LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(f->st, mask ? 0 : Ti, s); }));
+  if (mask) {
+    f->idx = reinterpret_cast<int*>(ws + L.idx);
+    uint16_t* h_c = reinterpret_cast<uint16_t*>(ws + L.h_c);
+    LMH_TRY(launch("compact", s, [&] {
+      return launch_compact(mask, targets, Ti, V, Ta, f->idx, f->y_c, f->st, s);
+    }));
+    LMH_TRY(launch("gather_rows", s, [&] {
+      return launch_gather_rows(hidden, H, f->idx, Ta, f->st, h_c, s);
+    }));
+    f->h_src = h_c;
+    f->rows_avail = f->T_alloc;
+  } else {
+    f->idx = nullptr;
+    LMH_TRY(launch("targets_dense", s, [&] {
+      return launch_targets_dense(targets, Ti, V, Ta, f->y_c, f->st, s);
+    }));
+    f->h_src = hidden;
+    f->rows_avail = T;
+  }
+  return LMHEAD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lmhead_workspace_size(int op, int64_t T, int32_t H, int32_t V, int32_t chunk_size) {
+  if ((op != LMHEAD_OP_FWD && op != LMHEAD_OP_BWD) ||
+      check_sizes(T, H, V, 1.0f, chunk_size) != LMHEAD_OK)
+    return 0;
+  return layout(op, T, H, V, chunk_size).total;
+}
+
+const char* lmhead_status_string(lmhead_status status) {
+  switch (status) {
+    case LMHEAD_OK: return "LMHEAD_OK";
+    case LMHEAD_ERR_INVALID_ARG: return "LMHEAD_ERR_INVALID_ARG: invalid argument";
+    case LMHEAD_ERR_UNSUPPORTED: return "LMHEAD_ERR_UNSUPPORTED: unsupported size or alignment";
+    case LMHEAD_ERR_WORKSPACE_TOO_SMALL: return "LMHEAD_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case LMHEAD_ERR_CUDA: return "LMHEAD_ERR_CUDA: CUDA launch or runtime error";
+    case LMHEAD_ERR_DEVICE_TIMEOUT: return "LMHEAD_ERR_DEVICE_TIMEOUT: a device wait exceeded its limit";
+    case LMHEAD_ERR_BAD_TARGET: return "LMHEAD_ERR_BAD_TARGET: a scored target lies outside [-V, V)";
+  }
+  return "unknown lmhead_status";
+}
+
+lmhead_status lmhead_plan_info(int64_t T, int32_t H, int32_t V, int32_t chunk_size,
+                               int32_t* fwd_splits, int32_t* bwd_tokens, int32_t* bwd_vocab) {
+  if (check_sizes(T, H, V, 1.0f, chunk_size) != LMHEAD_OK || T == 0) return LMHEAD_ERR_INVALID_ARG;
+  const int sms = sm_count();
+  if (fwd_splits)
+    *fwd_splits = sms > 0 ? choose_splits(ceil_div(T, BM), ceil_div(V, BN), sms) : 0;
+  const BwdPlan bp = plan_bwd(T, V, chunk_size);
+  if (bwd_tokens) *bwd_tokens = static_cast<int32_t>(bp.Tb);
+  if (bwd_vocab) *bwd_vocab = static_cast<int32_t>(bp.Vb);
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               float* logp, float* entropy, float* lse, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream) {
+  lmhead_status rc = check_sizes(T, H, V, temperature, chunk_size);
+  if (rc != LMHEAD_OK) return rc;
+  if (T == 0) return LMHEAD_OK;
+  if (!hidden || !weight || !targets || !logp || !lse || !workspace) return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return LMHEAD_ERR_UNSUPPORTED;
+  const Layout L = layout(LMHEAD_OP_FWD, T, H, V, chunk_size);
+  if (workspace_bytes < L.total) return LMHEAD_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return LMHEAD_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+
+  Front f;
+  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  if (rc != LMHEAD_OK) return rc;
+
+  const int64_t m_tiles = ceil_div(T, BM), n_tiles = ceil_div(V, BN);
+  const int splits = choose_splits(m_tiles, n_tiles, sms);
+  float4* part = reinterpret_cast<float4*>(ws + L.part);
+
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, f.h_src, H, f.rows_avail, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
+  if (!make_map(&mb, weight, H, V, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+
+  GemmArgs p{};
+  p.m_cap = static_cast<int>(T);
+  p.n_extent = V;
+  p.k_cap = H;
+  p.m_dynamic = 1;
+  p.dyn_base = 0;
+  p.dev_rows = &f.st->rows;
+  p.n_splits = splits;
+  p.status = &f.st->status;
+  p.scale = kLog2e / temperature;
+  p.y_c = f.y_c;
+  p.partials = part;
+  p.part_ld = static_cast<int>(f.T_alloc);
+  const int grid = static_cast<int>(std::min<int64_t>(m_tiles * splits, sms));
+  LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(ma, mb, p, grid, s); }));
+  LMH_TRY(launch("fwd_merge", s, [&] {
+    return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st,
+                            static_cast<int>(f.T_alloc), logp, entropy, lse, s);
+  }));
+  if (loss_mask) {
+    LMH_TRY(launch("zero_masked_outputs", s, [&] {
+      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse, s);
+    }));
+  }
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               const float* grad_logp, const float* grad_entropy,
+                               const float* lse, const float* entropy, float* d_hidden,
+                               float* d_weight, int accumulate_dweight, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream) {
+  lmhead_status rc = check_sizes(T, H, V, temperature, chunk_size);
+  if (rc != LMHEAD_OK) return rc;
+  if (!weight || !d_weight) return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(weight) || !aligned16(d_weight)) return LMHEAD_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (!accumulate_dweight &&
+        cudaMemsetAsync(d_weight, 0, sizeof(float) * static_cast<size_t>(V) * H, s) != cudaSuccess)
+      return LMHEAD_ERR_CUDA;
+    return LMHEAD_OK;
+  }
+  if (!hidden || !targets || !lse || !d_hidden || !workspace || (grad_entropy && !entropy))
+    return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(d_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return LMHEAD_ERR_UNSUPPORTED;
+  const Layout L = layout(LMHEAD_OP_BWD, T, H, V, chunk_size);
+  if (workspace_bytes < L.total) return LMHEAD_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = sm_count();
+  if (sms <= 0) return LMHEAD_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+
+  Front f;
+  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  if (rc != LMHEAD_OK) return rc;
+
+  float4* coef = reinterpret_cast<float4*>(ws + L.coef);
+  uint16_t* dz = reinterpret_cast<uint16_t*>(ws + L.dz);
+  LMH_TRY(launch("bwd_prep", s, [&] {
+    return launch_bwd_prep(f.idx, f.st, static_cast<int>(f.T_alloc), lse, entropy, grad_logp,
+                           grad_entropy, temperature, coef, s);
+  }));
+  if (loss_mask) {
+    LMH_TRY(launch("zero_masked_rows", s, [&] {
+      return launch_zero_masked_rows(loss_mask, static_cast<int>(T), H, d_hidden, s);
+    }));
+  }
+
+  const BwdPlan bp = plan_bwd(T, V, chunk_size);
+  const float scale = kLog2e / temperature;
+  for (int64_t tb = 0; tb < bp.n_tb; ++tb) {
+    const int64_t t0 = tb * bp.Tb;
+    if (t0 >= f.T_alloc) break;
+    const int64_t m_cap = std::min<int64_t>(bp.Tb, f.T_alloc - t0);
+    const int64_t h_rows = std::min<int64_t>(bp.Tb, f.rows_avail - t0);
+    const uint16_t* h_blk = f.h_src + t0 * H;
+    CUtensorMap h_kmaj, h_mn;
+    if (!make_map(&h_kmaj, h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
+    if (!make_map(&h_mn, h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+    for (int64_t vb = 0; vb < bp.n_vb; ++vb) {
+      const int64_t v0 = vb * bp.Vb;
+      if (v0 >= V) break;
+      const int64_t vact = std::min<int64_t>(bp.Vb, V - v0);
+      const uint16_t* w_blk = weight + v0 * H;
+      CUtensorMap w_kmaj, w_mn, dz_kmaj, dz_mn;
+      if (!make_map(&w_kmaj, w_blk, H, vact, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&w_mn, w_blk, H, vact, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&dz_kmaj, dz, vact, m_cap, 2ull * bp.Vb, BK, BM)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&dz_mn, dz, vact, m_cap, 2ull * bp.Vb, 64, 64)) return LMHEAD_ERR_CUDA;
+
+      // dz = cotangent of the recomputed logits of this block, bf16 scratch
+      GemmArgs pz{};
+      pz.m_cap = static_cast<int>(m_cap);
+      pz.n_extent = static_cast<int>(vact);
+      pz.k_cap = H;
+      pz.m_dynamic = 1;
+      pz.dyn_base = static_cast<int>(t0);
+      pz.dev_rows = &f.st->rows;
+      pz.status = &f.st->status;
+      pz.scale = scale;
+      pz.row_base = static_cast<int>(t0);
+      pz.col_base = static_cast<int>(v0);
+      pz.y_c = f.y_c;
+      pz.coef = coef;
+      pz.dz_out = dz;
+      pz.dz_ld = static_cast<int>(bp.Vb);
+      const int gz = static_cast<int>(
+          std::min<int64_t>(ceil_div(m_cap, BM) * ceil_div(vact, BN), sms));
+      LMH_TRY(launch("bwd_dz_gemm", s, [&] { return launch_gemm_bwd_dz(h_kmaj, w_kmaj, pz, gz, s); }));
+
+      // dh[block rows] (+)= dz . W_block
+      GemmArgs ph{};
+      ph.m_cap = static_cast<int>(m_cap);
+      ph.n_extent = H;
+      ph.k_cap = static_cast<int>(vact);
+      ph.m_dynamic = 1;
+      ph.dyn_base = static_cast<int>(t0);
+      ph.dev_rows = &f.st->rows;
+      ph.status = &f.st->status;
+      ph.row_base = static_cast<int>(t0);
+      ph.out = d_hidden;
+      ph.out_ld = H;
+      ph.row_map = f.idx;
+      ph.accumulate = vb > 0 ? 1 : 0;
+      const int gh = static_cast<int>(std::min<int64_t>(ceil_div(m_cap, BM) * ceil_div(H, BN), sms));
+      LMH_TRY(launch("bwd_dh_gemm", s, [&] { return launch_gemm_dh(dz_kmaj, w_mn, ph, gh, s); }));
+
+      // dW[block vocab rows] (+)= dz^T . h_block, token blocks in ascending order
+      GemmArgs pw{};
+      pw.m_cap = static_cast<int>(vact);
+      pw.n_extent = H;
+      pw.k_cap = static_cast<int>(m_cap);
+      pw.k_dynamic = 1;
+      pw.dyn_base = static_cast<int>(t0);
+      pw.dev_rows = &f.st->rows;
+      pw.status = &f.st->status;
+      pw.row_base = 0;
+      pw.out = d_weight + v0 * H;
+      pw.out_ld = H;
+      pw.accumulate = (tb > 0 || accumulate_dweight) ? 1 : 0;
+      pw.zero_if_empty = 1;
+      const int gw = static_cast<int>(std::min<int64_t>(ceil_div(vact, BM) * ceil_div(H, BN), sms));
+      LMH_TRY(launch("bwd_dw_gemm", s, [&] { return launch_gemm_dw(dz_mn, h_mn, pw, gw, s); }));
+    }
+  }
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream) {
+  if (!workspace) return LMHEAD_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return LMHEAD_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LMHEAD_ERR_CUDA;
+  return static_cast<lmhead_status>(v);
+}
+
+int64_t lmhead_read_scored_count(const void* workspace, lmhead_stream_t stream) {
+  if (!workspace) return -1;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  DeviceState st;
+  if (cudaMemcpy(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  return st.rows;
+}
+
+void lmhead_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on) {
+    for (ProfRecord& r : g_prof) {
+      cudaEventSynchronize(r.stop);
+      g_event_pool.push_back(r.start);
+      g_event_pool.push_back(r.stop);
+    }
+    g_prof.clear();
+  }
+  g_prof_on = on != 0;
+}
+
+int lmhead_profile_count(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  return static_cast<int>(g_prof.size());
+}
+
+lmhead_status lmhead_profile_record(int i, const char** name, float* ms) {
+  ProfRecord r;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (i < 0 || i >= static_cast<int>(g_prof.size())) return LMHEAD_ERR_INVALID_ARG;
+    r = g_prof[static_cast<size_t>(i)];
+  }
+  if (cudaEventSynchronize(r.stop) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  float t = 0.f;
+  if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) return LMHEAD_ERR_CUDA;
+  if (name) *name = r.name;
+  if (ms) *ms = t;
+  return LMHEAD_OK;
+}
+
+uint64_t lmhead_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

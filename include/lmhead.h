@@ -1,0 +1,189 @@
+/*
+ * lmhead.h -- C ABI of the chunked LM-head log-prob + entropy head for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * For every scored token t, with hidden row h_t (length H), vocabulary table
+ * W (V rows of length H), target id y_t and temperature tau:
+ *
+ *   z_v      = h_t . W_v / tau                         (v = 0 .. V-1)
+ *   lse_t    = log sum_v exp(z_v)
+ *   logp_t   = z_{y_t} - lse_t
+ *   entropy_t = lse_t - sum_v softmax(z)_v z_v         (nats)
+ *
+ * and the exact backward for per-token cotangents g_l (of logp) and g_e (of
+ * entropy):
+ *
+ *   dz_v        = g_l (onehot(y_t)_v - p_v) - g_e p_v (log p_v + entropy_t)
+ *   d_hidden_t  = sum_v (dz_v / tau) W_v
+ *   d_weight_v += sum_t (dz_v / tau) h_t
+ *
+ * Sources: the chunked LM head ("Compute cross-entropy loss in chunks
+ * instead of materializing the full logits tensor", SkyRL issue #891
+ * "[tx] support long sequence", section "What Each Optimization Does", item
+ * 4); the fused log-prob head (tunix PR #2913, commit "fused sharded
+ * log-prob head (TUNIX_LOGPS_SHARDED_HEAD=fused)" and section "How the fused
+ * log-prob head works": one pass over a chunk's logits gives the target
+ * logit by a one-hot select, the max and exp-sum, and the entropy from the
+ * same exponentials; the max and exp-sum are kept for the backward; the
+ * backward forms the logits' cotangent in one elementwise pass over
+ * recomputed logits and both gradient matmuls read that one cotangent);
+ * log-sum-exp merging of partial results ("Long Sequences (SeCO)",
+ * section "Efficiency").
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library allocates no device memory, never synchronises the stream in
+ *    the compute calls, and enqueues all work on `stream`.
+ *  - bf16 tensors are passed as raw bfloat16 bit patterns (uint16_t).
+ *  - Matrices are row-major and dense: hidden [T, H], weight [V, H],
+ *    d_hidden [T, H], d_weight [V, H].
+ *  - Argument errors are returned synchronously and nothing is launched:
+ *    LMHEAD_ERR_INVALID_ARG for a NULL required pointer, T < 0, H <= 0,
+ *    V <= 0, a temperature that is not finite and > 0, chunk_size <= 0;
+ *    LMHEAD_ERR_UNSUPPORTED for H not a multiple of 64, T >= 2^31 - 256,
+ *    or a bf16 / fp32 matrix pointer that is not 16-byte aligned;
+ *    LMHEAD_ERR_WORKSPACE_TOO_SMALL when workspace_bytes is below
+ *    lmhead_workspace_size().  A failed launch returns LMHEAD_ERR_CUDA.
+ *  - T == 0 is a no-op that returns LMHEAD_OK (the backward still zeroes
+ *    d_weight unless accumulate_dweight is set).
+ *  - Conditions found on the device (an unmasked target outside [-V, V), a
+ *    bounded wait that gave up) are recorded in a status word inside the
+ *    workspace; lmhead_read_device_status() returns it.
+ *  - Calls are reentrant as long as concurrent calls use distinct
+ *    workspaces.  Results are deterministic: the same inputs, shapes and
+ *    chunk_size give the same bits.
+ */
+#ifndef LMHEAD_H_
+#define LMHEAD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* lmhead_stream_t;
+
+typedef enum {
+  LMHEAD_OK = 0,
+  LMHEAD_ERR_INVALID_ARG = 1,
+  LMHEAD_ERR_UNSUPPORTED = 2,
+  LMHEAD_ERR_WORKSPACE_TOO_SMALL = 3,
+  LMHEAD_ERR_CUDA = 4,
+  LMHEAD_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait exceeded its limit */
+  LMHEAD_ERR_BAD_TARGET = 6      /* a scored target outside [-V, V) */
+} lmhead_status;
+
+enum { LMHEAD_OP_FWD = 0, LMHEAD_OP_BWD = 1 };
+
+/*
+ * Bytes of device workspace that lmhead_logps_fwd (op = LMHEAD_OP_FWD) or
+ * lmhead_logps_bwd (op = LMHEAD_OP_BWD) needs for these sizes; 0 for invalid
+ * sizes.  The workspace holds the compacted scored rows (2*T*H bytes at
+ * most), per-token statistics (tens of bytes per token) and, for the
+ * backward, a bf16 logit-cotangent block of at most about chunk_size * V
+ * elements.  It never grows with T * V: chunk_size alone bounds the
+ * vocabulary-wide scratch (SkyRL issue #891: the loss memory is set by the
+ * chunk, 300 MB at chunk_size 512 on a 152k vocabulary).
+ */
+size_t lmhead_workspace_size(int op, int64_t T, int32_t H, int32_t V, int32_t chunk_size);
+
+/*
+ * Forward: per-token log-prob of the target, entropy and log-sum-exp.
+ *
+ *  hidden     [T, H] bf16, weight [V, H] bf16
+ *  targets    [T] int32; ids in [-V, 0) wrap to id + V (tunix PR #2913,
+ *             _target_hit review thread); a scored id outside [-V, V) gives
+ *             logp = NaN and sets LMHEAD_ERR_BAD_TARGET in the device status
+ *  loss_mask  [T] uint8, nonzero = scored; NULL = every token scored.
+ *             Unscored tokens are skipped whole: their hidden rows are never
+ *             read by the GEMMs and their outputs are +0.0.
+ *  temperature  tau > 0; the logits are h.W / tau
+ *  chunk_size   tokens per chunk; sets the backward's scratch bound.  The
+ *             forward's results do not depend on it.
+ *  logp       [T] fp32 out
+ *  entropy    [T] fp32 out, or NULL to skip
+ *  lse        [T] fp32 out; keep it for lmhead_logps_bwd
+ *  workspace  device buffer of at least lmhead_workspace_size(LMHEAD_OP_FWD, ...)
+ *             bytes, 256-byte aligned
+ */
+lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               float* logp, float* entropy, float* lse, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream);
+
+/*
+ * Backward: exact d_hidden and d_weight for per-token cotangents.
+ *
+ *  hidden, weight, targets, loss_mask, T, H, V, temperature, chunk_size:
+ *             as given to lmhead_logps_fwd
+ *  grad_logp    [T] fp32 cotangent of logp, or NULL (zeros)
+ *  grad_entropy [T] fp32 cotangent of entropy, or NULL: the log-prob-only
+ *             backward (tunix PR #2913: GRPO stops the entropy's gradient)
+ *  lse        [T] fp32 from lmhead_logps_fwd (required)
+ *  entropy    [T] fp32 from lmhead_logps_fwd; required iff grad_entropy
+ *  d_hidden   [T, H] fp32 out, overwritten; unscored rows are +0.0
+ *  d_weight   [V, H] fp32 out; overwritten, or added to when
+ *             accumulate_dweight != 0 (micro-batch accumulation).  The
+ *             reduction over tokens runs in a fixed order (deterministic).
+ *  workspace  at least lmhead_workspace_size(LMHEAD_OP_BWD, ...) bytes
+ *
+ * The logits are recomputed chunk by chunk from hidden and weight; the
+ * logit cotangent is formed once per block and read by both gradient
+ * contractions.
+ */
+lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               const float* grad_logp, const float* grad_entropy,
+                               const float* lse, const float* entropy, float* d_hidden,
+                               float* d_weight, int accumulate_dweight, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device status word that the last
+ * call using `workspace` left (LMHEAD_OK, LMHEAD_ERR_BAD_TARGET or
+ * LMHEAD_ERR_DEVICE_TIMEOUT), or LMHEAD_ERR_CUDA if the read failed.
+ */
+lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream);
+
+/* Number of scored tokens found by the last call using `workspace`
+   (synchronises `stream`); -1 on error. */
+int64_t lmhead_read_scored_count(const void* workspace, lmhead_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* lmhead_status_string(lmhead_status status);
+
+/*
+ * Plan the library uses for these sizes on the current device:
+ *  fwd_splits   vocabulary splits per token block in the forward
+ *  bwd_tokens   tokens per backward block (T_b)
+ *  bwd_vocab    vocabulary rows per backward block (V_b); the bf16 cotangent
+ *               scratch holds bwd_tokens * bwd_vocab elements
+ * Returns LMHEAD_ERR_INVALID_ARG for invalid sizes.
+ */
+lmhead_status lmhead_plan_info(int64_t T, int32_t H, int32_t V, int32_t chunk_size,
+                               int32_t* fwd_splits, int32_t* bwd_tokens, int32_t* bwd_vocab);
+
+/*
+ * Instrumentation (off by default).  While enabled, every kernel launch is
+ * bracketed by CUDA events on its stream.  lmhead_profile_enable(1) clears
+ * earlier records.  lmhead_profile_record() synchronises on the i-th
+ * record's end event and returns its kernel name (static string) and
+ * duration in milliseconds.
+ */
+void lmhead_profile_enable(int on);
+int lmhead_profile_count(void);
+lmhead_status lmhead_profile_record(int i, const char** name, float* ms);
+
+/* Kernels this library has launched in this process. */
+uint64_t lmhead_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMHEAD_H_ */

@@ -1,0 +1,137 @@
+"""Host-side checks of the C ABI (CPU only: no kernel is launched).
+
+The library must load, export every entry point include/lmhead.h declares,
+size its workspace without any T x V term, and reject bad arguments
+synchronously with the documented status codes.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_lm_head_tcgen05_gb300 as lm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lmhead.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lm.build()
+    return lm.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmhead_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lm._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in lm.STATUS_NAMES.items():
+        assert lm.lmhead_status_string(code).startswith(name)
+    assert "unknown" in lm.lmhead_status_string(99)
+
+
+def test_workspace_size_invalid(lib):
+    assert lm.lmhead_workspace_size(0, -1, 64, 10, 8) == 0
+    assert lm.lmhead_workspace_size(0, 10, 0, 10, 8) == 0
+    assert lm.lmhead_workspace_size(0, 10, 64, 0, 8) == 0
+    assert lm.lmhead_workspace_size(0, 10, 64, 10, 0) == 0
+    assert lm.lmhead_workspace_size(0, 10, 65, 10, 8) == 0     # H % 64 != 0
+    assert lm.lmhead_workspace_size(2, 10, 64, 10, 8) == 0     # unknown op
+
+
+@pytest.mark.parametrize("T,H,V,c", [(4096, 2560, 151936, 512), (65536, 2560, 151936, 512),
+                                     (65536, 4096, 151936, 4096), (200000, 2048, 151936, 4096),
+                                     (256, 128, 2048, 64), (1, 64, 1, 1)])
+def test_workspace_bounded_by_chunk(lib, T, H, V, c):
+    """No T x V term: fwd is O(T (H + splits)), bwd adds at most ~chunk*V bf16."""
+    Ta = (T + 127) // 128 * 128
+    fwd = lm.lmhead_workspace_size(0, T, H, V, c)
+    bwd = lm.lmhead_workspace_size(1, T, H, V, c)
+    per_token = 4 + 4 + 2 * H
+    assert 0 < fwd <= Ta * (per_token + 16 * 32) + 8 * 256
+    dz_bound = 2 * max(c * V, 128 * 256) + 2 * 128 * 256 * max(1, V // 256) * 0
+    # the scratch block is T_b x V_b bf16 with T_b * V_b <= chunk * V (+ rounding of one tile)
+    assert bwd <= Ta * (per_token + 16) + 2 * (c * V + 128 * 256 + 256 * Ta + 128 * V) + 8 * 256
+    assert bwd < 2 * T * V or T * V < 1 << 20
+    del dz_bound
+
+
+def _fake(n):
+    return ctypes.c_void_p(n)
+
+
+def test_forward_argument_errors(lib):
+    f = lib.lmhead_logps_fwd
+    A = _fake(1 << 20)
+    ws = _fake(1 << 24)
+    ok_args = dict(T=8, H=64, V=10, tau=1.0, c=4)
+
+    def call(h=A, w=A, y=A, m=None, T=8, H=64, V=10, tau=1.0, c=4, lp=A, en=None, ls=A,
+             wsp=ws, wsb=1 << 40):
+        return f(h, w, y, m, T, H, V, tau, c, lp, en, ls, wsp, wsb, None)
+
+    assert call(T=-1) == 1
+    assert call(H=0) == 1
+    assert call(V=0) == 1
+    assert call(c=0) == 1
+    assert call(tau=0.0) == 1
+    assert call(tau=float("nan")) == 1
+    assert call(tau=float("inf")) == 1
+    assert call(tau=-0.5) == 1
+    assert call(H=96) == 2
+    assert call(T=0, h=None, w=None, y=None, lp=None, ls=None, wsp=None) == 0   # no-op
+    assert call(h=None) == 1
+    assert call(w=None) == 1
+    assert call(y=None) == 1
+    assert call(lp=None) == 1
+    assert call(ls=None) == 1
+    assert call(wsp=None) == 1
+    assert call(h=_fake((1 << 20) + 8)) == 2      # misaligned bf16 matrix
+    assert call(wsp=_fake((1 << 24) + 16)) == 2   # workspace not 256-aligned
+    assert call(wsb=16) == 3
+    del ok_args
+
+
+def test_backward_argument_errors(lib):
+    f = lib.lmhead_logps_bwd
+    A = _fake(1 << 20)
+    ws = _fake(1 << 24)
+
+    def call(h=A, w=A, y=A, m=None, T=8, H=64, V=10, tau=1.0, c=4, gl=A, ge=None, ls=A, en=None,
+             dh=A, dw=A, acc=0, wsp=ws, wsb=1 << 40):
+        return f(h, w, y, m, T, H, V, tau, c, gl, ge, ls, en, dh, dw, acc, wsp, wsb, None)
+
+    assert call(T=-3) == 1
+    assert call(H=-64) == 1
+    assert call(tau=0.0) == 1
+    assert call(H=32) == 2
+    assert call(dw=None) == 1
+    assert call(ls=None) == 1
+    assert call(dh=None) == 1
+    assert call(ge=A, en=None) == 1          # entropy is required with grad_entropy
+    assert call(dh=_fake((1 << 20) + 4)) == 2
+    assert call(dw=_fake((1 << 20) + 4)) == 2
+    assert call(wsb=100) == 3
+    assert call(T=0, acc=1, h=None, y=None, ls=None, dh=None, wsp=None) == 0
+
+
+def test_plan_is_chunk_bounded(lib):
+    """T_b * V_b never exceeds chunk_size * V beyond one tile of rounding."""
+    for T, V, c in [(4096, 151936, 512), (65536, 151936, 512), (65536, 151936, 4096),
+                    (200000, 151936, 4096), (256, 2048, 64), (300, 3001, 16), (5, 7, 1)]:
+        _, tb, vb = lm.lmhead_plan_info(T, 128, V, c)
+        assert tb % 128 == 0 and vb % 256 == 0
+        assert tb * vb <= max(c * V, 128 * 256) + 128 * 256 + 256 * tb + 128 * vb, (T, V, c, tb, vb)
+        assert tb <= (T + 127) // 128 * 128
