@@ -1,0 +1,383 @@
+"""Benchmark: fused log-prob + entropy forward + backward of the chunked LM head.
+
+One step = lmhead_logps_fwd + lmhead_logps_bwd (logp, entropy, lse, then
+d_hidden and d_weight for per-token cotangents of logp and entropy) over one
+batch of the workload, through the C ABI.  Default workload: the
+Qwen3-4B-shaped head (T = 4096 tokens, H = 2560, V = 151,936, chunk 512,
+tau = 1) with synthetic seeded inputs.
+
+Prints ONE JSON line (rank 0).  `value` is tokens/s with inputs resident in
+HBM; `e2e` is the same metric with the per-step inputs copied from pinned
+host memory and the per-token results copied back inside the timed region.
+`roofline` reports the dominant kernel's achieved TFLOP/s (algorithmic flops
+per launch / mean launch time from CUDA events on the launching stream)
+against the measured dense BF16 peak.  `cpu_baseline` times the fp64 oracle
+on a bounded sample of the same workload on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  (N > 1: launched by torch.distributed.run, one independent replica per GPU)
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and TFLOP/s of fused logp+entropy fwd+bwd; % of GB300 BF16 tensor peak"
+UNIT = "tokens/s"
+GEMM_KERNELS = ("fwd_stats_gemm", "bwd_dz_gemm", "bwd_dh_gemm", "bwd_dw_gemm")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_4b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_setup(n):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_inputs(name):
+    from chunked_lm_head_tcgen05_gb300 import workloads
+    w = workloads.WORKLOADS[name]
+    return w, workloads.make_inputs(w)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit())
+        mx = max((float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_lm_head_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class OracleSample:
+    """The fp64 oracle, as it stands, on the first n tokens of the workload:
+    full forward + backward (d_hidden rows and every d_weight row)."""
+
+    def __init__(self, name):
+        import oracle
+        from chunked_lm_head_tcgen05_gb300 import workloads
+        self.w, x = workload_inputs(name)
+        self.o = oracle.default()
+        self.hb = workloads.bf16_bits(x["hidden"])
+        self.wb = workloads.bf16_bits(x["weight"])
+        self.y = x["targets"].numpy()
+        self.m = None if x["loss_mask"] is None else x["loss_mask"].numpy()
+        self.gl = x["grad_logp"].double().numpy()
+        self.ge = x["grad_entropy"].double().numpy()
+
+    def run(self, n):
+        """Returns (scored tokens, seconds) for one pass over n tokens."""
+        import numpy as np
+        mm = None if self.m is None else self.m[:n]
+        t0 = time.perf_counter()
+        self.o.forward(self.hb[:n], self.wb, self.y[:n], mm, self.w.temperature)
+        self.o.backward(self.hb[:n], self.wb, self.y[:n], mm, self.w.temperature, self.gl[:n],
+                        self.ge[:n])
+        dt = time.perf_counter() - t0
+        return (n if mm is None else int(np.sum(mm != 0))), dt
+
+    def calibrate(self, seconds):
+        """Smallest power-of-two sample that takes about `seconds` (at least 1 token)."""
+        T = self.w.T
+        n = 1
+        _, dt = self.run(n)
+        while dt < seconds / 2 and n < min(4096, T):
+            n = min(2 * n, T)
+            _, dt = self.run(n)
+        return n
+
+    def describe(self, n, dt):
+        return ("first %d tokens of the %s workload: fp64 forward + backward (all %d d_weight "
+                "rows), %.2f s per pass" % (n, self.w.name, self.w.V, dt))
+
+
+def cpu_baseline(name, seconds):
+    s = OracleSample(name)
+    n = s.calibrate(seconds)
+    scored, dt = s.run(n)
+    return {"value": scored / dt, "unit": UNIT, "cores": s.o.num_threads(), "kind": "oracle",
+            "sample": s.describe(n, dt)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one pass over a fixed
+    sample, sized so that warm-up + timed steps take about two minutes."""
+    if rank != 0:
+        return
+    s = OracleSample(args.workload)
+    n = s.calibrate(max(0.5, 120.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        s.run(n)
+    tok, sec = 0, 0.0
+    for _ in range(args.steps):
+        a, dt = s.run(n)
+        tok += a
+        sec += dt
+    v = tok / sec
+    w = s.w
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "%s: T=%d, H=%d, V=%d, chunk=%d, tau=%g"
+                   % (w.name, w.T, w.H, w.V, w.chunk_size, w.temperature)},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": s.o.num_threads(), "kind": "oracle",
+                         "sample": s.describe(n, sec / args.steps)},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import chunked_lm_head_tcgen05_gb300 as lm
+    lm.build()
+    lm.library()
+    w, x = workload_inputs(args.workload)
+    dev = torch.device("cuda", local)
+    T, H, V = w.T, w.H, w.V
+    c, tau = w.chunk_size, w.temperature
+    g = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    from chunked_lm_head_tcgen05_gb300 import workloads
+    Tv = workloads.scored_count(x)
+    logp = torch.empty(T, device=dev)
+    ent = torch.empty(T, device=dev)
+    lse = torch.empty(T, device=dev)
+    dh = torch.empty((T, H), device=dev)
+    dw = torch.empty((V, H), device=dev)
+    ws = torch.empty(max(lm.lmhead_workspace_size(0, T, H, V, c),
+                         lm.lmhead_workspace_size(1, T, H, V, c)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(src):
+        rc = lm.lmhead_logps_fwd(src["hidden"], g["weight"], src["targets"], src["loss_mask"], tau,
+                                 c, logp, ent, lse, ws, stream)
+        rc |= lm.lmhead_logps_bwd(src["hidden"], g["weight"], src["targets"], src["loss_mask"],
+                                  tau, c, src["grad_logp"], src["grad_entropy"], lse, ent, dh, dw,
+                                  0, ws, stream)
+        if rc:
+            raise lm.LmheadError(rc, "step")
+
+    def timed(fn, k):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        step(g)
+    torch.cuda.synchronize()
+    assert lm.lmhead_read_device_status(ws, stream) == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    n0 = lm.lmhead_launch_count()
+    t = timed(lambda: step(g), args.steps)
+    launches = lm.lmhead_launch_count() - n0
+    clk = clocks.stop()
+    t = max_over_ranks(t, world)
+    ms = t / args.steps * 1e3
+    value = Tv * world * args.steps / t
+
+    # ---- per-kernel durations (CUDA events around each launch, same stream)
+    lm.lmhead_profile_enable(1)
+    timed(lambda: step(g), max(3, args.steps // 4))
+    lm.lmhead_profile_enable(0)
+    per = {}
+    for i in range(lm.lmhead_profile_count()):
+        name, kms = lm.lmhead_profile_record(i)
+        a = per.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += kms
+    total_ms = sum(v[1] for v in per.values())
+    n_prof_steps = max(3, args.steps // 4)
+    flops_per_gemm_step = 2.0 * Tv * H * V
+    dom = max(GEMM_KERNELS, key=lambda k: per.get(k, [0, 0.0])[1])
+    dl, dms = per[dom]
+    launches_per_step = dl / n_prof_steps
+    flops_per_launch = flops_per_gemm_step / launches_per_step
+    achieved = flops_per_launch / (dms / dl / 1e3) / 1e12
+    peaks, src = measured_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(dom, args.workload),
+                "peak_source": "%s bf16_tflops_sustained (of %s)" % ("MEASURED_PEAKS.json", src),
+                "flops_per_launch": flops_per_launch, "launches_per_step": launches_per_step}
+    kernels = {k: {"launches_per_step": v[0] / n_prof_steps, "ms_per_step": v[1] / n_prof_steps,
+                   "share": v[1] / total_ms} for k, v in sorted(per.items())}
+
+    # ---- end to end: per-step inputs from pinned host memory, results back
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()
+            if k in ("hidden", "targets", "loss_mask", "grad_logp", "grad_entropy")}
+    staged = {k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else None)
+              for k, v in host.items()}
+    out_logp = torch.empty(T, dtype=torch.float32).pin_memory()
+    out_ent = torch.empty(T, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+    d2h = 2 * T * 4
+
+    def e2e_step():
+        for k, v in host.items():
+            if isinstance(v, torch.Tensor):
+                staged[k].copy_(v, non_blocking=True)
+        step(staged)
+        out_logp.copy_(logp, non_blocking=True)
+        out_ent.copy_(ent, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    te = max_over_ranks(timed(e2e_step, max(3, args.steps // 2)), world)
+    e2e_value = Tv * world * max(3, args.steps // 2) / te
+
+    counted = 6.0 * Tv * H * V
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: T=%d (scored %d), H=%d, V=%d, chunk=%d, tau=%g"
+                   % (w.name, T, Tv, H, V, c, w.temperature),
+                   "T": T, "H": H, "V": V, "chunk_size": c, "temperature": tau,
+                   "l2": "inputs larger than L2 (weight %.0f MB bf16 streamed every step)"
+                         % (V * H * 2 / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops_counted": counted * world / (t / args.steps) / 1e12,
+        "tflops_executed": 8.0 * Tv * H * V * world / (t / args.steps) / 1e12,
+        "frac_peak_counted": counted / (t / args.steps) / 1e12 / peak,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roofline,
+        "kernels": kernels,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
