@@ -36,7 +36,7 @@ GEMM_KERNELS = ("fwd_stats_gemm", "bwd_dz_gemm", "bwd_dh_gemm", "bwd_dw_gemm")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=150)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_4b")
@@ -124,7 +124,7 @@ class ClockSampler:
         sm = sorted(float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit())
         mx = max((float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()), default=None)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
                 "reasons": reasons, "samples": len(rows)}
 
