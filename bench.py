@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--workload", default="qwen3_4b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only-device", action="store_true",
+                    help="time the device-resident steps only (profiling runs)")
     return ap.parse_args()
 
 
@@ -288,6 +290,12 @@ def run_ours(args, rank, world, local):
     t = max_over_ranks(t, world)
     ms = t / args.steps * 1e3
     value = Tv * world * args.steps / t
+
+    if args.only_device:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": ms,
+                              "steps": args.steps, "warmup": args.warmup, "only_device": True}))
+        return
 
     # ---- per-kernel durations (CUDA events around each launch, same stream)
     lm.lmhead_profile_enable(1)

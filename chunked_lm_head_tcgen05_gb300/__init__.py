@@ -19,11 +19,13 @@ __all__ = [
     "lmhead_workspace_size", "lmhead_logps_fwd", "lmhead_logps_bwd",
     "lmhead_read_device_status", "lmhead_read_scored_count", "lmhead_status_string",
     "lmhead_plan_info", "lmhead_profile_enable", "lmhead_profile_count",
-    "lmhead_profile_record", "lmhead_launch_count", "forward", "backward",
+    "lmhead_profile_record", "lmhead_launch_count", "lmhead_logps_fwd_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "forward", "backward",
 ]
 
 LMHEAD_OP_FWD = 0
 LMHEAD_OP_BWD = 1
+NOALLOC_SCRATCH_BYTES = 64 << 20   # LMHEAD_NOALLOC_SCRATCH_BYTES in include/lmhead.h
 STATUS_NAMES = {
     0: "LMHEAD_OK", 1: "LMHEAD_ERR_INVALID_ARG", 2: "LMHEAD_ERR_UNSUPPORTED",
     3: "LMHEAD_ERR_WORKSPACE_TOO_SMALL", 4: "LMHEAD_ERR_CUDA",
@@ -57,6 +59,8 @@ _SIGNATURES = {
     "lmhead_profile_record": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                                              ctypes.POINTER(ctypes.c_float)]),
     "lmhead_launch_count": (ctypes.c_uint64, []),
+    "lmhead_logps_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32,
+                                                ctypes.c_float, _I32, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -163,6 +167,28 @@ def lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size
         int(chunk_size), _ptr(grad_logp), _ptr(grad_entropy), _ptr(lse), _ptr(entropy),
         _ptr(d_hidden), _ptr(d_weight), int(bool(accumulate_dweight)), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lmhead_logps_fwd_noalloc(hidden, weight, targets, loss_mask, temperature, chunk_size, logp,
+                             entropy, lse, stream=None):
+    """C ``lmhead_logps_fwd_noalloc`` on torch tensors; returns the status code.
+
+    For callers that cannot allocate device memory: no workspace argument,
+    the scratch is the library's static per-GPU array (up to
+    LMHEAD_NOALLOC_SCRATCH_BYTES of forward workspace)."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight, "weight", torch.bfloat16, (V, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(logp, "logp", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    return int(library().lmhead_logps_fwd_noalloc(
+        _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
+        int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _stream(stream)))
 
 
 def lmhead_read_device_status(workspace, stream=None):

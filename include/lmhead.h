@@ -154,6 +154,43 @@ lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t s
    (synchronises `stream`); -1 on error. */
 int64_t lmhead_read_scored_count(const void* workspace, lmhead_stream_t stream);
 
+/*
+ * Size of the static device scratch that lmhead_logps_fwd_noalloc uses:
+ * 64 MiB, held on every GPU that loads this library until the process exits.
+ */
+#define LMHEAD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Forward without a caller workspace, for callers that cannot allocate
+ * device memory: a plugin running inside a host program that owns every
+ * device allocation and hands it no allocator, or code on a path where a
+ * cudaMalloc would synchronise the device and stall other work.  The pages
+ * have no counterpart to this entry point; it exists only for such callers.
+ *
+ * Same arguments, results and errors as lmhead_logps_fwd, minus the
+ * workspace: the scratch comes from one file-scope device array of
+ * LMHEAD_NOALLOC_SCRATCH_BYTES per GPU.  It allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library call).
+ *  - Sizes whose forward workspace (lmhead_workspace_size(LMHEAD_OP_FWD,
+ *    ...)) exceeds LMHEAD_NOALLOC_SCRATCH_BYTES are rejected with
+ *    LMHEAD_ERR_WORKSPACE_TOO_SMALL before anything is launched (about
+ *    11,000 tokens at H = 2560).
+ *  - The first call on a device looks up the array's device address on the
+ *    current device (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; each call re-initialises the parts that must start
+ *    from a known state.  Calls whose work overlaps on the GPU (different
+ *    streams, or different host threads without ordering) race on it.
+ *  - lmhead_read_device_status cannot see this scratch; check logp for NaN
+ *    to detect invalid targets.
+ */
+lmhead_status lmhead_logps_fwd_noalloc(const uint16_t* hidden, const uint16_t* weight,
+                                       const int32_t* targets, const uint8_t* loss_mask,
+                                       int64_t T, int32_t H, int32_t V, float temperature,
+                                       int32_t chunk_size, float* logp, float* entropy,
+                                       float* lse, lmhead_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* lmhead_status_string(lmhead_status status);
 
