@@ -30,7 +30,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s and TFLOP/s of fused logp+entropy fwd+bwd; % of GB300 BF16 tensor peak"
 UNIT = "tokens/s"
-GEMM_KERNELS = ("fwd_stats_gemm", "bwd_dz_gemm", "bwd_dh_gemm", "bwd_dw_gemm")
+# GEMM kernels and their algorithmic flops per step in units of T_v*H*V
+GEMM_KERNELS = {"fwd_stats_gemm": 2.0, "bwd_dz_gemm": 2.0, "bwd_grad_gemm": 4.0}
 
 
 def parse():
@@ -309,11 +310,10 @@ def run_ours(args, rank, world, local):
         a[1] += kms
     total_ms = sum(v[1] for v in per.values())
     n_prof_steps = max(3, args.steps // 4)
-    flops_per_gemm_step = 2.0 * Tv * H * V
     dom = max(GEMM_KERNELS, key=lambda k: per.get(k, [0, 0.0])[1])
     dl, dms = per[dom]
     launches_per_step = dl / n_prof_steps
-    flops_per_launch = flops_per_gemm_step / launches_per_step
+    flops_per_launch = GEMM_KERNELS[dom] * Tv * H * V / launches_per_step
     achieved = flops_per_launch / (dms / dl / 1e3) / 1e12
     peaks, src = measured_peaks()
     peak = peaks["bf16_tflops_sustained"]

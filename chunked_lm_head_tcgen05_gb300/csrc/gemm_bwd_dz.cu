@@ -1,11 +1,11 @@
-// Instantiation of the tcgen05 GEMM for the backward logit recompute GEMM with the dz epilogue (A = hidden rows, B = vocabulary rows, both K-major).
+// Instantiation of the tcgen05 GEMM for the backward logit recompute with
+// the dz epilogue (A = hidden rows, B = vocabulary rows, both K-major).
 #include "tc_gemm.cuh"
 
 namespace lmh {
 
-cudaError_t launch_gemm_bwd_dz(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p,
-                               int grid, cudaStream_t s) {
-  return launch_tc_gemm<EPI_BWD_DZ, false, false>(a, b, p, grid, s);
+cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, cudaStream_t s) {
+  return launch_tc_gemm<EPI_BWD_DZ, false>(a, grid, s);
 }
 
 }  // namespace lmh

@@ -69,17 +69,30 @@ struct GemmArgs {
   int zero_if_empty;     // EPI_STORE_F32: K == 0 and !accumulate writes zeros
 };
 
+// One launch of the tensor-core GEMM runs one or two problems (GEMMs with
+// the same epilogue kind).  Work units of problem 0 come first, then those of
+// problem 1; CTAs fetch units from a device counter (zeroed before the
+// launch), so units with long K (put first) start first and short ones fill
+// the tail.
+constexpr int MAX_PROBLEMS = 2;
+
+struct Problem {
+  GemmArgs p;
+  int a_mn;   // 1: the A operand is MN-major in memory (B majorness is a template flag)
+};
+
+struct LaunchArgs {
+  CUtensorMap map_a[MAX_PROBLEMS];
+  CUtensorMap map_b[MAX_PROBLEMS];
+  Problem prob[MAX_PROBLEMS];
+  int n_problems;
+  int* counter;
+};
+
 // Launchers.  Each returns the launch error (cudaSuccess when enqueued).
-// A and B are described by TMA maps built on the host; a_mn / b_mn select
-// MN-major operand layouts.
-cudaError_t launch_gemm_fwd_stats(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p,
-                                  int grid, cudaStream_t s);
-cudaError_t launch_gemm_bwd_dz(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p,
-                               int grid, cudaStream_t s);
-cudaError_t launch_gemm_dh(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p, int grid,
-                           cudaStream_t s);
-cudaError_t launch_gemm_dw(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p, int grid,
-                           cudaStream_t s);
+cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, cudaStream_t s);
 
 // Auxiliary kernels (aux.cu).
 cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,

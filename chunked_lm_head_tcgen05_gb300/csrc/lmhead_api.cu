@@ -178,7 +178,8 @@ BwdPlan plan_bwd(int64_t T, int64_t V, int64_t chunk) {
 }
 
 struct Layout {
-  size_t state, idx, y_c, h_c, part, coef, dz, total;
+  size_t state, counters, idx, y_c, h_c, part, coef, dz, total;
+  int64_t n_counters;   // dynamic work-unit counters, one per GEMM launch
 };
 
 Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
@@ -191,6 +192,13 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
     return o;
   };
   L.state = take(sizeof(DeviceState));
+  if (op == LMHEAD_OP_FWD) {
+    L.n_counters = 1;
+  } else {
+    const BwdPlan bp = plan_bwd(T, V, chunk);
+    L.n_counters = 2 * bp.n_tb * bp.n_vb;
+  }
+  L.counters = take(4 * static_cast<size_t>(L.n_counters));
   L.idx = take(4 * static_cast<size_t>(T_alloc));
   L.y_c = take(4 * static_cast<size_t>(T_alloc));
   L.h_c = take(2 * static_cast<size_t>(T_alloc) * static_cast<size_t>(H));
@@ -223,6 +231,7 @@ lmhead_status check_sizes(int64_t T, int32_t H, int32_t V, float tau, int32_t ch
 // wrap, and the gather of scored rows.  Sets the row source for the GEMMs.
 struct Front {
   DeviceState* st;
+  int* counters;        // zeroed work-unit counters, one per GEMM launch
   int* idx;             // NULL when every token is scored
   int* y_c;
   const uint16_t* h_src;
@@ -236,6 +245,9 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
   f->st = reinterpret_cast<DeviceState*>(ws + L.state);
   f->y_c = reinterpret_cast<int*>(ws + L.y_c);
   const int Ti = static_cast<int>(T), Ta = static_cast<int>(f->T_alloc);
+  f->counters = reinterpret_cast<int*>(ws + L.counters);
+  if (cudaMemsetAsync(f->counters, 0, 4 * static_cast<size_t>(L.n_counters), s) != cudaSuccess)
+    return LMHEAD_ERR_CUDA;
   LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(f->st, mask ? 0 : Ti, s); }));
   if (mask) {
     f->idx = reinterpret_cast<int*>(ws + L.idx);
@@ -321,11 +333,11 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   const int splits = choose_splits(m_tiles, n_tiles, sms);
   float4* part = reinterpret_cast<float4*>(ws + L.part);
 
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, f.h_src, H, f.rows_avail, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-  if (!make_map(&mb, weight, H, V, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
-
-  GemmArgs p{};
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  if (!make_map(&la.map_a[0], f.h_src, H, f.rows_avail, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
+  if (!make_map(&la.map_b[0], weight, H, V, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+  GemmArgs& p = la.prob[0].p;
   p.m_cap = static_cast<int>(T);
   p.n_extent = V;
   p.k_cap = H;
@@ -338,8 +350,10 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   p.y_c = f.y_c;
   p.partials = part;
   p.part_ld = static_cast<int>(f.T_alloc);
+  la.n_problems = 1;
+  la.counter = f.counters;
   const int grid = static_cast<int>(std::min<int64_t>(m_tiles * splits, sms));
-  LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(ma, mb, p, grid, s); }));
+  LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(la, grid, s); }));
   LMH_TRY(launch("fwd_merge", s, [&] {
     return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st,
                             static_cast<int>(f.T_alloc), logp, entropy, lse, s);
@@ -404,22 +418,19 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
     const int64_t m_cap = std::min<int64_t>(bp.Tb, f.T_alloc - t0);
     const int64_t h_rows = std::min<int64_t>(bp.Tb, f.rows_avail - t0);
     const uint16_t* h_blk = f.h_src + t0 * H;
-    CUtensorMap h_kmaj, h_mn;
-    if (!make_map(&h_kmaj, h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-    if (!make_map(&h_mn, h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
     for (int64_t vb = 0; vb < bp.n_vb; ++vb) {
       const int64_t v0 = vb * bp.Vb;
       if (v0 >= V) break;
       const int64_t vact = std::min<int64_t>(bp.Vb, V - v0);
       const uint16_t* w_blk = weight + v0 * H;
-      CUtensorMap w_kmaj, w_mn, dz_kmaj, dz_mn;
-      if (!make_map(&w_kmaj, w_blk, H, vact, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&w_mn, w_blk, H, vact, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&dz_kmaj, dz, vact, m_cap, 2ull * bp.Vb, BK, BM)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&dz_mn, dz, vact, m_cap, 2ull * bp.Vb, 64, 64)) return LMHEAD_ERR_CUDA;
+      int* counter = f.counters + 2 * (tb * bp.n_vb + vb);
 
       // dz = cotangent of the recomputed logits of this block, bf16 scratch
-      GemmArgs pz{};
+      LaunchArgs lz;
+      std::memset(&lz, 0, sizeof(lz));
+      if (!make_map(&lz.map_a[0], h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&lz.map_b[0], w_blk, H, vact, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+      GemmArgs& pz = lz.prob[0].p;
       pz.m_cap = static_cast<int>(m_cap);
       pz.n_extent = static_cast<int>(vact);
       pz.k_cap = H;
@@ -434,12 +445,20 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       pz.coef = coef;
       pz.dz_out = dz;
       pz.dz_ld = static_cast<int>(bp.Vb);
+      lz.n_problems = 1;
+      lz.counter = counter;
       const int gz = static_cast<int>(
           std::min<int64_t>(ceil_div(m_cap, BM) * ceil_div(vact, BN), sms));
-      LMH_TRY(launch("bwd_dz_gemm", s, [&] { return launch_gemm_bwd_dz(h_kmaj, w_kmaj, pz, gz, s); }));
+      LMH_TRY(launch("bwd_dz_gemm", s, [&] { return launch_gemm_bwd_dz(lz, gz, s); }));
 
-      // dh[block rows] (+)= dz . W_block
-      GemmArgs ph{};
+      // one launch for both gradient contractions of the block
+      LaunchArgs lg;
+      std::memset(&lg, 0, sizeof(lg));
+      // problem 0: dh[block rows] (+)= dz . W_block   (K = vocabulary of the block)
+      if (!make_map(&lg.map_a[0], dz, vact, m_cap, 2ull * bp.Vb, BK, BM)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&lg.map_b[0], w_blk, H, vact, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+      GemmArgs& ph = lg.prob[0].p;
+      lg.prob[0].a_mn = 0;
       ph.m_cap = static_cast<int>(m_cap);
       ph.n_extent = H;
       ph.k_cap = static_cast<int>(vact);
@@ -452,11 +471,11 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       ph.out_ld = H;
       ph.row_map = f.idx;
       ph.accumulate = vb > 0 ? 1 : 0;
-      const int gh = static_cast<int>(std::min<int64_t>(ceil_div(m_cap, BM) * ceil_div(H, BN), sms));
-      LMH_TRY(launch("bwd_dh_gemm", s, [&] { return launch_gemm_dh(dz_kmaj, w_mn, ph, gh, s); }));
-
-      // dW[block vocab rows] (+)= dz^T . h_block, token blocks in ascending order
-      GemmArgs pw{};
+      // problem 1: dW[block vocab rows] (+)= dz^T . h_block (K = tokens, ascending blocks)
+      if (!make_map(&lg.map_a[1], dz, vact, m_cap, 2ull * bp.Vb, 64, 64)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+      GemmArgs& pw = lg.prob[1].p;
+      lg.prob[1].a_mn = 1;
       pw.m_cap = static_cast<int>(vact);
       pw.n_extent = H;
       pw.k_cap = static_cast<int>(m_cap);
@@ -469,8 +488,11 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       pw.out_ld = H;
       pw.accumulate = (tb > 0 || accumulate_dweight) ? 1 : 0;
       pw.zero_if_empty = 1;
-      const int gw = static_cast<int>(std::min<int64_t>(ceil_div(vact, BM) * ceil_div(H, BN), sms));
-      LMH_TRY(launch("bwd_dw_gemm", s, [&] { return launch_gemm_dw(dz_mn, h_mn, pw, gw, s); }));
+      lg.n_problems = 2;
+      lg.counter = counter + 1;
+      const int gg = static_cast<int>(std::min<int64_t>(
+          (ceil_div(m_cap, BM) + ceil_div(vact, BM)) * ceil_div(H, BN), sms));
+      LMH_TRY(launch("bwd_grad_gemm", s, [&] { return launch_gemm_bwd_grad(lg, gg, s); }));
     }
   }
   return LMHEAD_OK;

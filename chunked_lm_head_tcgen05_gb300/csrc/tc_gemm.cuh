@@ -2,19 +2,26 @@
 // chunked LM head (sm_103a).
 //
 // One CTA per SM, 192 threads:
-//   warp 0      TMA producer (one elected lane): A and B tiles into a
-//               4-stage shared-memory ring, 128-byte swizzled.
+//   warp 0      scheduler + TMA producer (one elected lane): fetches work
+//               units from a device counter, passes each unit index to the
+//               other roles through a small shared-memory ring, and streams
+//               the unit's A and B tiles into a 4-stage shared-memory ring,
+//               128-byte swizzled.
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
 //               accumulators) and issues tcgen05.mma (one elected lane).
 //   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane)
 //               and reads it 32 columns at a time with tcgen05.ld.
-// Accumulators are double buffered, so the epilogue of one tile overlaps
-// the MMAs of the next.
+// Accumulators are double buffered, so the epilogue of one tile overlaps the
+// MMAs of the next.
 //
-// Work units: a unit is one 128-row block of M and a contiguous range of
-// 256-column N tiles.  For the forward statistics the range is a vocabulary
-// split (the running softmax statistics stay in registers across it); for
-// every other epilogue a unit is one tile.  CTAs take units round robin.
+// A launch holds one or two problems (see LaunchArgs).  A work unit is one
+// 128-row block of M and a contiguous range of 256-column N tiles: for the
+// forward statistics the range is a vocabulary split (the running softmax
+// statistics stay in registers across it); otherwise a unit is one tile.
+// Units of problem 0 are numbered first.  Fetching units dynamically keeps
+// every SM busy until the end when units differ in length or in speed.
+// Every unit is computed entirely by one CTA in a fixed order, so results do
+// not depend on which CTA took it.
 //
 // Every wait on an mbarrier is bounded (about 2 s of wall time); when one
 // gives up the CTA records STATUS_DEVICE_TIMEOUT in the device status word,
@@ -27,14 +34,17 @@
 namespace lmh {
 
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
-constexpr float LOG2E_F = 1.4426950408889634f;
+constexpr int SCHED_DEPTH = 4;
 
 struct SharedCtl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t sfull[SCHED_DEPTH];
+  uint64_t sempty[SCHED_DEPTH];
   uint64_t drain;
+  int sched[SCHED_DEPTH];
   uint32_t tmem_base;
   int abort;
 };
@@ -90,19 +100,36 @@ struct Sched {
   }
 };
 
-template <int EPI, bool A_MN, bool B_MN>
+// Global unit index -> (problem, unit within it).
+__device__ __forceinline__ int split_unit(const Sched* sc, int u, int& q) {
+  if (u < sc[0].units) {
+    q = 0;
+    return u;
+  }
+  q = 1;
+  return u - sc[0].units;
+}
+
+template <int EPI, bool B_MN>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, const GemmArgs p) {
+    tc_gemm_kernel(const __grid_constant__ LaunchArgs L) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  int* const status = L.prob[0].p.status;
 
-  Sched sc;
-  sc.init(p);
+  Sched sc[MAX_PROBLEMS];
+  sc[0].init(L.prob[0].p);
+  if (L.n_problems > 1) {
+    sc[1].init(L.prob[1].p);
+  } else {
+    sc[1] = sc[0];
+    sc[1].units = 0;
+  }
+  const int total_units = sc[0].units + sc[1].units;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -112,6 +139,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->tfull[b]), 1);
       mbar_init(smem_addr(&ctl->tempty[b]), EPI_WARPS);
+    }
+    for (int s = 0; s < SCHED_DEPTH; ++s) {
+      mbar_init(smem_addr(&ctl->sfull[s]), 1);
+      mbar_init(smem_addr(&ctl->sempty[s]), 1 + EPI_WARPS);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
@@ -129,38 +160,58 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t smem_base = smem_addr(smem);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && sc.k_blocks > 0) {
-      tma_prefetch_map(&map_a);
-      tma_prefetch_map(&map_b);
+    // ------------------------------------------------------ scheduler + producer
+    if (lane == 0) {
+      for (int q = 0; q < L.n_problems; ++q) {
+        tma_prefetch_map(&L.map_a[q]);
+        tma_prefetch_map(&L.map_b[q]);
+      }
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sc.units; u += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        const int slot = i & (SCHED_DEPTH - 1);
+        const uint32_t spar = (i / SCHED_DEPTH) & 1;
+        if (!wait_bounded(smem_addr(&ctl->sempty[slot]), spar ^ 1, abort, status)) {
+          ok = false;
+          break;
+        }
+        int u = atomicAdd(L.counter, 1);
+        if (u >= total_units) u = -1;
+        ctl->sched[slot] = u;
+        mbar_arrive(smem_addr(&ctl->sfull[slot]));
+        if (u < 0) break;
+        int q;
+        const int lu = split_unit(sc, u, q);
+        const Sched& s = sc[q];
+        if (s.k_blocks == 0) continue;
+        const CUtensorMap* ma = &L.map_a[q];
+        const CUtensorMap* mb = &L.map_b[q];
+        const bool a_mn = L.prob[q].a_mn != 0;
         int m, split, nb, ne;
-        sc.unit(u, m, split, nb, ne);
+        s.unit(lu, m, split, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
-          for (int kb = 0; kb < sc.k_blocks; ++kb) {
+          for (int kb = 0; kb < s.k_blocks; ++kb) {
             const uint32_t fb = smem_addr(&ctl->full[stage]);
-            if (!wait_bounded(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, p.status)) {
+            if (!wait_bounded(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(fb, STAGE_BYTES);
             const uint32_t sa = smem_base + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_TILE_BYTES;
-            if (!A_MN) {
-              tma_load_2d(sa, &map_a, fb, kb * BK, m * BM);
+            if (!a_mn) {
+              tma_load_2d(sa, ma, fb, kb * BK, m * BM);
             } else {
-              tma_load_2d(sa, &map_a, fb, m * BM, kb * BK);
-              tma_load_2d(sa + 8192, &map_a, fb, m * BM + 64, kb * BK);
+              tma_load_2d(sa, ma, fb, m * BM, kb * BK);
+              tma_load_2d(sa + 8192, ma, fb, m * BM + 64, kb * BK);
             }
             if (!B_MN) {
-              tma_load_2d(sb, &map_b, fb, kb * BK, n * BN);
+              tma_load_2d(sb, mb, fb, kb * BK, n * BN);
             } else {
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i)
-                tma_load_2d(sb + i * 8192, &map_b, fb, n * BN + 64 * i, kb * BK);
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * 8192, mb, fb, n * BN + 64 * j, kb * BK);
             }
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -178,22 +229,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && sc.k_blocks > 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    if (lane == 0) {
+      constexpr uint32_t IDESC_AK = idesc_bf16_f32(BM, BN, false, B_MN);
+      constexpr uint32_t IDESC_AMN = idesc_bf16_f32(BM, BN, true, B_MN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sc.units; u += gridDim.x) {
+      for (int i = 0; ok; ++i) {
+        const int slot = i & (SCHED_DEPTH - 1);
+        const uint32_t spar = (i / SCHED_DEPTH) & 1;
+        if (!wait_bounded(smem_addr(&ctl->sfull[slot]), spar, abort, status)) {
+          ok = false;
+          break;
+        }
+        const int u = ctl->sched[slot];
+        mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        if (u < 0) break;
+        int q;
+        const int lu = split_unit(sc, u, q);
+        const Sched& s = sc[q];
+        if (s.k_blocks == 0) continue;
+        const bool a_mn = L.prob[q].a_mn != 0;
+        const uint32_t idesc = a_mn ? IDESC_AMN : IDESC_AK;
         int m, split, nb, ne;
-        sc.unit(u, m, split, nb, ne);
+        s.unit(lu, m, split, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
-          if (!wait_bounded(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, p.status)) {
+          if (!wait_bounded(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          for (int kb = 0; kb < sc.k_blocks; ++kb) {
-            if (!wait_bounded(smem_addr(&ctl->full[stage]), phase, abort, p.status)) {
+          for (int kb = 0; kb < s.k_blocks; ++kb) {
+            if (!wait_bounded(smem_addr(&ctl->full[stage]), phase, abort, status)) {
               ok = false;
               break;
             }
@@ -203,12 +270,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               // K-major: the next 16 K elements are 32 bytes further along the
-              // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further.
-              const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+              // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further,
+              // with the 64-wide MN chunks 8 KB apart.
+              const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
               const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
             umma_commit(smem_addr(&ctl->empty[stage]));
             if (++stage == STAGES) {
@@ -229,19 +297,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;            // TMEM lane quarter this warp may read
-    const int lrow = q * 32 + lane;    // accumulator row of this thread
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int qw = warp & 3;            // TMEM lane quarter this warp may read
+    const int lrow = qw * 32 + lane;    // accumulator row of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     uint32_t acc = 0, acc_phase = 0;
 
-    if (sc.k_blocks == 0) {
-      if constexpr (EPI == EPI_STORE_F32) {
-        if (p.zero_if_empty && !p.accumulate) {
-          for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
-            int m, split, nb, ne;
-            sc.unit(u, m, split, nb, ne);
-            const int row = m * BM + lrow;
-            if (row >= sc.M) continue;
+    for (int i = 0;; ++i) {
+      const int slot = i & (SCHED_DEPTH - 1);
+      const uint32_t spar = (i / SCHED_DEPTH) & 1;
+      int u = 0;
+      uint32_t got = 1;
+      if (lane == 0) {
+        got = wait_bounded(smem_addr(&ctl->sfull[slot]), spar, abort, status) ? 1u : 0u;
+        if (got) u = ctl->sched[slot];
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[slot]));
+      if (u < 0) break;
+      int q;
+      const int lu = split_unit(sc, u, q);
+      const Sched& s = sc[q];
+      const GemmArgs& p = L.prob[q].p;
+      int m, split, nb, ne;
+      s.unit(lu, m, split, nb, ne);
+      const int row = m * BM + lrow;
+
+      if (s.k_blocks == 0) {
+        if constexpr (EPI == EPI_STORE_F32) {
+          if (p.zero_if_empty && !p.accumulate && row < s.M) {
             const int64_t orow = p.row_map ? p.row_map[p.row_base + row] : p.row_base + row;
             for (int n = nb; n < ne; ++n) {
               float* dst = p.out + orow * p.out_ld + n * BN;
@@ -250,168 +335,163 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         }
+        continue;
       }
-    } else {
-      for (int u = blockIdx.x; u < sc.units; u += gridDim.x) {
-        int m, split, nb, ne;
-        sc.unit(u, m, split, nb, ne);
-        const int row = m * BM + lrow;
 
-        // per-unit state
-        float mrun = -INFINITY, ssum = 0.f, s1 = 0.f, zy = -INFINITY;   // EPI_FWD_STATS
-        float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);                   // EPI_BWD_DZ
-        int y = -1;
-        bool row_ok = false;
-        int64_t orow = 0;
-        if constexpr (EPI == EPI_FWD_STATS) {
-          row_ok = row < sc.M;
-          if (row_ok) y = p.y_c[p.row_base + row];
-        } else if constexpr (EPI == EPI_BWD_DZ) {
-          row_ok = row < p.m_cap;
-          if (row_ok) {
-            cf = p.coef[p.row_base + row];
-            y = p.y_c[p.row_base + row];
-          }
-        } else {
-          row_ok = row < sc.M;
-          if (row_ok) orow = p.row_map ? p.row_map[p.row_base + row] : p.row_base + row;
+      // per-unit state
+      float mrun = -INFINITY, ssum = 0.f, s1 = 0.f, zy = -INFINITY;   // EPI_FWD_STATS
+      float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);                   // EPI_BWD_DZ
+      int y = -1;
+      bool row_ok = false;
+      int64_t orow = 0;
+      if constexpr (EPI == EPI_FWD_STATS) {
+        row_ok = row < s.M;
+        if (row_ok) y = p.y_c[p.row_base + row];
+      } else if constexpr (EPI == EPI_BWD_DZ) {
+        row_ok = row < p.m_cap;
+        if (row_ok) {
+          cf = p.coef[p.row_base + row];
+          y = p.y_c[p.row_base + row];
         }
+      } else {
+        row_ok = row < s.M;
+        if (row_ok) orow = p.row_map ? p.row_map[p.row_base + row] : p.row_base + row;
+      }
 
-        bool ok = true;
-        for (int n = nb; n < ne; ++n) {
-          uint32_t got = 1;
-          if (lane == 0)
-            got = wait_bounded(smem_addr(&ctl->tfull[acc]), acc_phase, abort, p.status) ? 1u : 0u;
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const int col0 = n * BN;
-          const uint32_t tcol = tmem_base + lane_off + acc * BN;
-          const int yt = y - p.col_base - col0;
+      bool ok = true;
+      for (int n = nb; n < ne; ++n) {
+        uint32_t t_ok = 1;
+        if (lane == 0)
+          t_ok = wait_bounded(smem_addr(&ctl->tfull[acc]), acc_phase, abort, status) ? 1u : 0u;
+        t_ok = __shfl_sync(0xffffffffu, t_ok, 0);
+        if (!t_ok) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const int col0 = n * BN;
+        const uint32_t tcol = tmem_base + lane_off + acc * BN;
+        const int yt = y - p.col_base - col0;
 
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_load_32(tcol + c * 32, v);
-            if (c == BN / 32 - 1) {
-              // the accumulator is fully read: hand it back to the MMA warp
-              tc_fence_before_sync();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty[acc]));
-            }
-            const int cb = c * 32;
-            const int lim = p.n_extent - col0 - cb;   // valid columns in this chunk
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_load_32(tcol + c * 32, v);
+          if (c == BN / 32 - 1) {
+            // the accumulator is fully read: hand it back to the MMA warp
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty[acc]));
+          }
+          const int cb = c * 32;
+          const int lim = p.n_extent - col0 - cb;   // valid columns in this chunk
 
-            if constexpr (EPI == EPI_FWD_STATS) {
-              float cmax = -INFINITY;
-              if (lim >= 32) {
+          if constexpr (EPI == EPI_FWD_STATS) {
+            float cmax = -INFINITY;
+            if (lim >= 32) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
-              } else {
+              for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+            } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < lim) cmax = fmaxf(cmax, v[j]);
+              for (int j = 0; j < 32; ++j)
+                if (j < lim) cmax = fmaxf(cmax, v[j]);
+            }
+            const float cm = cmax * p.scale;
+            if (cm > mrun) {
+              const float dm = mrun - cm;
+              const float r = ex2_approx(dm);
+              s1 = ssum > 0.f ? r * fmaf(dm, ssum, s1) : 0.f;
+              ssum *= r;
+              mrun = cm;
+            }
+            if (lim >= 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float d = fmaf(v[j], p.scale, -mrun);
+                const float e = ex2_approx(d);
+                ssum += e;
+                s1 = fmaf(e, d, s1);
               }
-              const float cm = cmax * p.scale;
-              if (cm > mrun) {
-                const float dm = mrun - cm;
-                const float r = ex2_approx(dm);
-                s1 = ssum > 0.f ? r * fmaf(dm, ssum, s1) : 0.f;
-                ssum *= r;
-                mrun = cm;
-              }
-              if (lim >= 32) {
+            } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+              for (int j = 0; j < 32; ++j) {
+                if (j < lim) {
                   const float d = fmaf(v[j], p.scale, -mrun);
                   const float e = ex2_approx(d);
                   ssum += e;
                   s1 = fmaf(e, d, s1);
                 }
+              }
+            }
+            if (static_cast<unsigned>(yt - cb) < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == yt - cb) zy = v[j] * p.scale;
+            }
+          } else if constexpr (EPI == EPI_BWD_DZ) {
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float d = fmaf(v[j], p.scale, -cf.x);
+              const float pr = ex2_approx(d);
+              g[j] = -pr * fmaf(cf.y, d, cf.z);
+            }
+            if (static_cast<unsigned>(yt - cb) < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == yt - cb) g[j] += cf.w;
+            }
+            if (row_ok && lim > 0) {
+              uint16_t* dst = p.dz_out + static_cast<int64_t>(row) * p.dz_ld + col0 + cb;
+              uint32_t pk[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
+              if (lim >= 32) {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
               } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  if (j < lim) {
-                    const float d = fmaf(v[j], p.scale, -mrun);
-                    const float e = ex2_approx(d);
-                    ssum += e;
-                    s1 = fmaf(e, d, s1);
-                  }
-                }
+                for (int j = 0; j < 32; ++j)
+                  if (j < lim)
+                    dst[j] = static_cast<uint16_t>((j & 1) ? (pk[j >> 1] >> 16)
+                                                           : (pk[j >> 1] & 0xFFFFu));
               }
-              if (static_cast<unsigned>(yt - cb) < 32u) {
+            }
+          } else {
+            if (row_ok && lim > 0) {
+              float* dst = p.out + orow * p.out_ld + col0 + cb;
+              if (lim >= 32) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                  if (p.accumulate) {
+                    const float4 old = d4[k];
+                    o.x += old.x;
+                    o.y += old.y;
+                    o.z += old.z;
+                    o.w += old.w;
+                  }
+                  d4[k] = o;
+                }
+              } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                  if (j == yt - cb) zy = v[j] * p.scale;
-              }
-            } else if constexpr (EPI == EPI_BWD_DZ) {
-              float g[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float d = fmaf(v[j], p.scale, -cf.x);
-                const float pr = ex2_approx(d);
-                g[j] = -pr * fmaf(cf.y, d, cf.z);
-              }
-              if (static_cast<unsigned>(yt - cb) < 32u) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j == yt - cb) g[j] += cf.w;
-              }
-              if (row_ok && lim > 0) {
-                uint16_t* dst = p.dz_out + static_cast<int64_t>(row) * p.dz_ld + col0 + cb;
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
-                if (lim >= 32) {
-                  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-                  for (int i = 0; i < 4; ++i)
-                    d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j)
-                    if (j < lim)
-                      dst[j] = static_cast<uint16_t>((j & 1) ? (pk[j >> 1] >> 16)
-                                                             : (pk[j >> 1] & 0xFFFFu));
-                }
-              }
-            } else {
-              if (row_ok && lim > 0) {
-                float* dst = p.out + orow * p.out_ld + col0 + cb;
-                if (lim >= 32) {
-                  float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    if (p.accumulate) {
-                      const float4 old = d4[i];
-                      o.x += old.x;
-                      o.y += old.y;
-                      o.z += old.z;
-                      o.w += old.w;
-                    }
-                    d4[i] = o;
-                  }
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j)
-                    if (j < lim) dst[j] = p.accumulate ? dst[j] + v[j] : v[j];
-                }
+                  if (j < lim) dst[j] = p.accumulate ? dst[j] + v[j] : v[j];
               }
             }
           }
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
         }
-        if (!ok) break;
-        if constexpr (EPI == EPI_FWD_STATS) {
-          if (row_ok)
-            p.partials[static_cast<int64_t>(split) * p.part_ld + row] =
-                make_float4(mrun, ssum, s1, zy);
-        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) break;
+      if constexpr (EPI == EPI_FWD_STATS) {
+        if (row_ok)
+          p.partials[static_cast<int64_t>(split) * p.part_ld + row] =
+              make_float4(mrun, ssum, s1, zy);
       }
     }
   }
@@ -424,14 +504,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN>
-cudaError_t launch_tc_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& p, int grid,
-                           cudaStream_t s) {
-  auto kern = tc_gemm_kernel<EPI, A_MN, B_MN>;
+template <int EPI, bool B_MN>
+cudaError_t launch_tc_gemm(const LaunchArgs& a, int grid, cudaStream_t s) {
+  auto kern = tc_gemm_kernel<EPI, B_MN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(GEMM_SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(a, b, p);
+  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(a);
   return cudaGetLastError();
 }
 

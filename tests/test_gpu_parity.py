@@ -179,6 +179,6 @@ def test_instrumentation_counts_and_names():
     n = lm.lmhead_profile_count()
     names = [lm.lmhead_profile_record(i)[0] for i in range(n)]
     assert lm.lmhead_launch_count() - n0 == n
-    for k in ("fwd_stats_gemm", "fwd_merge", "bwd_dz_gemm", "bwd_dh_gemm", "bwd_dw_gemm"):
+    for k in ("fwd_stats_gemm", "fwd_merge", "bwd_dz_gemm", "bwd_grad_gemm"):
         assert k in names
     assert all(lm.lmhead_profile_record(i)[1] >= 0 for i in range(n))
