@@ -4,8 +4,9 @@
 
 namespace lmh {
 
-cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, cudaStream_t s) {
-  return launch_tc_gemm<EPI_BWD_DZ, false>(a, grid, s);
+cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, bool pair, cudaStream_t s) {
+  return pair ? launch_tc_gemm<EPI_BWD_DZ, false, true>(a, grid, s)
+              : launch_tc_gemm<EPI_BWD_DZ, false, false>(a, grid, s);
 }
 
 }  // namespace lmh

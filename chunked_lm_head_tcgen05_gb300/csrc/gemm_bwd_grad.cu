@@ -8,8 +8,9 @@
 
 namespace lmh {
 
-cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, cudaStream_t s) {
-  return launch_tc_gemm<EPI_STORE_F32, true>(a, grid, s);
+cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, bool pair, cudaStream_t s) {
+  return pair ? launch_tc_gemm<EPI_STORE_F32, true, true>(a, grid, s)
+              : launch_tc_gemm<EPI_STORE_F32, true, false>(a, grid, s);
 }
 
 }  // namespace lmh

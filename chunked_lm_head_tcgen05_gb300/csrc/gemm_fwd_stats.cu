@@ -5,8 +5,9 @@
 
 namespace lmh {
 
-cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, cudaStream_t s) {
-  return launch_tc_gemm<EPI_FWD_STATS, false>(a, grid, s);
+cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, bool pair, cudaStream_t s) {
+  return pair ? launch_tc_gemm<EPI_FWD_STATS, false, true>(a, grid, s)
+              : launch_tc_gemm<EPI_FWD_STATS, false, false>(a, grid, s);
 }
 
 }  // namespace lmh

@@ -90,9 +90,12 @@ struct LaunchArgs {
 };
 
 // Launchers.  Each returns the launch error (cudaSuccess when enqueued).
-cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, cudaStream_t s);
+// pair = true runs each tile on a cluster of two CTAs (tcgen05 cta_group::2,
+// 256-row units, B staged half per CTA); the B maps must then use 128-row
+// K-major boxes.  `grid` is the number of CTAs wanted.
+cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
+cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
+cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
 
 // Auxiliary kernels (aux.cu).
 cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,

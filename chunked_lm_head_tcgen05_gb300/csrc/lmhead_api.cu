@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -81,6 +82,19 @@ int sm_count() {
   if (dev >= 0 && dev < 64) cache[dev] = n;
   return n;
 }
+
+// Tiles run on CTA pairs (tcgen05 cta_group::2) unless the environment sets
+// LMHEAD_CTA_PAIR=0 (single-CTA tiles; a diagnostic fallback).
+bool use_pair() {
+  static const bool on = [] {
+    const char* e = std::getenv("LMHEAD_CTA_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+int unit_rows() { return use_pair() ? 2 * BM : BM; }
+uint32_t b_box_rows() { return use_pair() ? BN / 2 : BN; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -300,7 +314,9 @@ lmhead_status lmhead_plan_info(int64_t T, int32_t H, int32_t V, int32_t chunk_si
   if (check_sizes(T, H, V, 1.0f, chunk_size) != LMHEAD_OK || T == 0) return LMHEAD_ERR_INVALID_ARG;
   const int sms = sm_count();
   if (fwd_splits)
-    *fwd_splits = sms > 0 ? choose_splits(ceil_div(T, BM), ceil_div(V, BN), sms) : 0;
+    *fwd_splits = sms > 0 ? choose_splits(ceil_div(T, unit_rows()), ceil_div(V, BN),
+                                          use_pair() ? sms / 2 : sms)
+                          : 0;
   const BwdPlan bp = plan_bwd(T, V, chunk_size);
   if (bwd_tokens) *bwd_tokens = static_cast<int32_t>(bp.Tb);
   if (bwd_vocab) *bwd_vocab = static_cast<int32_t>(bp.Vb);
@@ -329,14 +345,15 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
   if (rc != LMHEAD_OK) return rc;
 
-  const int64_t m_tiles = ceil_div(T, BM), n_tiles = ceil_div(V, BN);
-  const int splits = choose_splits(m_tiles, n_tiles, sms);
+  const bool pair = use_pair();
+  const int64_t m_tiles = ceil_div(T, unit_rows()), n_tiles = ceil_div(V, BN);
+  const int splits = choose_splits(m_tiles, n_tiles, pair ? sms / 2 : sms);
   float4* part = reinterpret_cast<float4*>(ws + L.part);
 
   LaunchArgs la;
   std::memset(&la, 0, sizeof(la));
   if (!make_map(&la.map_a[0], f.h_src, H, f.rows_avail, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-  if (!make_map(&la.map_b[0], weight, H, V, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+  if (!make_map(&la.map_b[0], weight, H, V, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
   GemmArgs& p = la.prob[0].p;
   p.m_cap = static_cast<int>(T);
   p.n_extent = V;
@@ -352,8 +369,8 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   p.part_ld = static_cast<int>(f.T_alloc);
   la.n_problems = 1;
   la.counter = f.counters;
-  const int grid = static_cast<int>(std::min<int64_t>(m_tiles * splits, sms));
-  LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(la, grid, s); }));
+  const int grid = static_cast<int>(std::min<int64_t>(m_tiles * splits * (pair ? 2 : 1), sms));
+  LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(la, grid, pair, s); }));
   LMH_TRY(launch("fwd_merge", s, [&] {
     return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st,
                             static_cast<int>(f.T_alloc), logp, entropy, lse, s);
@@ -412,6 +429,9 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
 
   const BwdPlan bp = plan_bwd(T, V, chunk_size);
   const float scale = kLog2e / temperature;
+  const bool pair = use_pair();
+  const int64_t um = unit_rows();
+  const int64_t ctas = pair ? 2 : 1;
   for (int64_t tb = 0; tb < bp.n_tb; ++tb) {
     const int64_t t0 = tb * bp.Tb;
     if (t0 >= f.T_alloc) break;
@@ -429,7 +449,7 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       LaunchArgs lz;
       std::memset(&lz, 0, sizeof(lz));
       if (!make_map(&lz.map_a[0], h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&lz.map_b[0], w_blk, H, vact, 2ull * H, BK, BN)) return LMHEAD_ERR_CUDA;
+      if (!make_map(&lz.map_b[0], w_blk, H, vact, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
       GemmArgs& pz = lz.prob[0].p;
       pz.m_cap = static_cast<int>(m_cap);
       pz.n_extent = static_cast<int>(vact);
@@ -448,8 +468,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       lz.n_problems = 1;
       lz.counter = counter;
       const int gz = static_cast<int>(
-          std::min<int64_t>(ceil_div(m_cap, BM) * ceil_div(vact, BN), sms));
-      LMH_TRY(launch("bwd_dz_gemm", s, [&] { return launch_gemm_bwd_dz(lz, gz, s); }));
+          std::min<int64_t>(ceil_div(m_cap, um) * ceil_div(vact, BN) * ctas, sms));
+      LMH_TRY(launch("bwd_dz_gemm", s, [&] { return launch_gemm_bwd_dz(lz, gz, pair, s); }));
 
       // one launch for both gradient contractions of the block
       LaunchArgs lg;
@@ -491,8 +511,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       lg.n_problems = 2;
       lg.counter = counter + 1;
       const int gg = static_cast<int>(std::min<int64_t>(
-          (ceil_div(m_cap, BM) + ceil_div(vact, BM)) * ceil_div(H, BN), sms));
-      LMH_TRY(launch("bwd_grad_gemm", s, [&] { return launch_gemm_bwd_grad(lg, gg, s); }));
+          (ceil_div(m_cap, um) + ceil_div(vact, um)) * ceil_div(H, BN) * ctas, sms));
+      LMH_TRY(launch("bwd_grad_gemm", s, [&] { return launch_gemm_bwd_grad(lg, gg, pair, s); }));
     }
   }
   return LMHEAD_OK;

@@ -1,11 +1,11 @@
 // Persistent, warp-specialised tcgen05 GEMM with fused epilogues for the
 // chunked LM head (sm_103a).
 //
-// One CTA per SM, 192 threads:
+// Per CTA, 192 threads:
 //   warp 0      scheduler + TMA producer (one elected lane): fetches work
 //               units from a device counter, passes each unit index to the
 //               other roles through a small shared-memory ring, and streams
-//               the unit's A and B tiles into a 4-stage shared-memory ring,
+//               the unit's A and B tiles into a shared-memory ring,
 //               128-byte swizzled.
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
 //               accumulators) and issues tcgen05.mma (one elected lane).
@@ -14,18 +14,27 @@
 // Accumulators are double buffered, so the epilogue of one tile overlaps the
 // MMAs of the next.
 //
+// PAIR = true runs the same roles on a cluster of two CTAs (two SMs) that
+// share one 256 x 256 output tile: each CTA stages its own 128 rows of A and
+// half (128 columns) of B, the even CTA issues tcgen05.mma.cta_group::2
+// (M = 256) over both CTAs' shared memory, and each CTA's TMEM receives its
+// 128 rows of D.  Per SM this halves the B traffic and the B staging space,
+// so six stages fit instead of four.  The even CTA fetches the work units and
+// forwards them to its peer; the peer's loads complete on the even CTA's
+// barriers, and MMA completion is multicast back to both CTAs.
+//
 // A launch holds one or two problems (see LaunchArgs).  A work unit is one
-// 128-row block of M and a contiguous range of 256-column N tiles: for the
-// forward statistics the range is a vocabulary split (the running softmax
-// statistics stay in registers across it); otherwise a unit is one tile.
-// Units of problem 0 are numbered first.  Fetching units dynamically keeps
-// every SM busy until the end when units differ in length or in speed.
-// Every unit is computed entirely by one CTA in a fixed order, so results do
-// not depend on which CTA took it.
+// block of M rows (128, or 256 for a pair) and a contiguous range of
+// 256-column N tiles: for the forward statistics the range is a vocabulary
+// split (the running softmax statistics stay in registers across it);
+// otherwise a unit is one tile.  Units of problem 0 are numbered first.
+// Fetching units dynamically keeps every SM busy until the end when units
+// differ in length or speed.  Every unit is computed entirely by one CTA (or
+// pair) in a fixed order, so results do not depend on who took it.
 //
 // Every wait on an mbarrier is bounded (about 2 s of wall time); when one
 // gives up the CTA records STATUS_DEVICE_TIMEOUT in the device status word,
-// drains its in-flight copies and MMAs, frees TMEM and exits.
+// lets its in-flight copies and MMAs finish, frees TMEM and exits.
 #pragma once
 
 #include "kernels.h"
@@ -35,10 +44,23 @@ namespace lmh {
 
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int SCHED_DEPTH = 4;
+constexpr int MAX_STAGES = 6;
+
+template <bool PAIR>
+struct TileCfg {
+  static constexpr int CTAS = PAIR ? 2 : 1;
+  static constexpr int UNIT_M = BM * CTAS;            // output rows per work unit
+  static constexpr int B_ROWS = BN / CTAS;            // N columns of B staged per CTA
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
+  static constexpr uint32_t STAGE = A_TILE_BYTES + B_BYTES;
+  static constexpr int NSTAGE = PAIR ? 6 : 4;
+  static_assert(NSTAGE * STAGE <= STAGES * STAGE_BYTES, "stage ring exceeds the shared memory plan");
+  static_assert(NSTAGE <= MAX_STAGES, "too many stages");
+};
 
 struct SharedCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t sfull[SCHED_DEPTH];
@@ -48,17 +70,23 @@ struct SharedCtl {
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(SharedCtl) <= 256, "control block exceeds its shared memory slot");
 
 // Wait for `parity` on `bar`; false if it gave up (time limit, or another
-// role of this CTA gave up first).
+// role of this CTA gave up first).  CLUSTER selects acquire at cluster scope
+// (the barrier is also arrived on by the peer CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                              int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() {
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
       *abort = 1;
@@ -76,16 +104,22 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
 struct Sched {
   int M, K, m_tiles, n_tiles, n_splits, k_blocks, units;
 
-  __device__ __forceinline__ void init(const GemmArgs& p) {
+  __device__ __forceinline__ void init(const GemmArgs& p, int unit_m) {
     int dev = 0;
     if (p.m_dynamic || p.k_dynamic) dev = *p.dev_rows - p.dyn_base;
     dev = dev < 0 ? 0 : dev;
     M = p.m_dynamic ? min(dev, p.m_cap) : p.m_cap;
     K = p.k_dynamic ? min(dev, p.k_cap) : p.k_cap;
-    m_tiles = (M + BM - 1) / BM;
+    m_tiles = (M + unit_m - 1) / unit_m;
     n_tiles = (p.n_extent + BN - 1) / BN;
     n_splits = p.n_splits > 0 ? min(p.n_splits, n_tiles) : n_tiles;
     k_blocks = (K + BK - 1) / BK;
@@ -110,9 +144,10 @@ __device__ __forceinline__ int split_unit(const Sched* sc, int u, int& q) {
   return u - sc[0].units;
 }
 
-template <int EPI, bool B_MN>
+template <int EPI, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ LaunchArgs L) {
+  using C = TileCfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -120,11 +155,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int* const status = L.prob[0].p.status;
+  const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
+  const bool leader = rank == 0;
 
   Sched sc[MAX_PROBLEMS];
-  sc[0].init(L.prob[0].p);
+  sc[0].init(L.prob[0].p, C::UNIT_M);
   if (L.n_problems > 1) {
-    sc[1].init(L.prob[1].p);
+    sc[1].init(L.prob[1].p, C::UNIT_M);
   } else {
     sc[1] = sc[0];
     sc[1].units = 0;
@@ -132,32 +169,51 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int total_units = sc[0].units + sc[1].units;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->tfull[b]), 1);
-      mbar_init(smem_addr(&ctl->tempty[b]), EPI_WARPS);
+      mbar_init(smem_addr(&ctl->tempty[b]), EPI_WARPS * C::CTAS);
     }
     for (int s = 0; s < SCHED_DEPTH; ++s) {
       mbar_init(smem_addr(&ctl->sfull[s]), 1);
-      mbar_init(smem_addr(&ctl->sempty[s]), 1 + EPI_WARPS);
+      mbar_init(smem_addr(&ctl->sempty[s]), (1 + EPI_WARPS) * C::CTAS);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_addr(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
   const uint32_t smem_base = smem_addr(smem);
+
+  // scheduler ring: the even CTA fetches, the odd CTA reads its copy
+  auto sched_take = [&](int slot, uint32_t spar, int& u) -> bool {
+    if (!wait_bounded<PAIR>(smem_addr(&ctl->sfull[slot]), spar, abort, status)) return false;
+    u = ctl->sched[slot];
+    return true;
+  };
+  auto sched_release = [&](int slot) {
+    if (PAIR && !leader)
+      mbar_arrive_remote(map_to_cta(smem_addr(&ctl->sempty[slot]), 0));
+    else
+      mbar_arrive(smem_addr(&ctl->sempty[slot]));
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ scheduler + producer
@@ -172,14 +228,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int i = 0; ok; ++i) {
         const int slot = i & (SCHED_DEPTH - 1);
         const uint32_t spar = (i / SCHED_DEPTH) & 1;
-        if (!wait_bounded(smem_addr(&ctl->sempty[slot]), spar ^ 1, abort, status)) {
-          ok = false;
-          break;
+        int u;
+        if (leader) {
+          if (!wait_bounded<PAIR>(smem_addr(&ctl->sempty[slot]), spar ^ 1, abort, status)) {
+            ok = false;
+            break;
+          }
+          u = atomicAdd(L.counter, 1);
+          if (u >= total_units) u = -1;
+          ctl->sched[slot] = u;
+          if constexpr (PAIR) {
+            st_shared_remote(map_to_cta(smem_addr(&ctl->sched[slot]), 1), u);
+            mbar_arrive_remote(map_to_cta(smem_addr(&ctl->sfull[slot]), 1));
+          }
+          mbar_arrive(smem_addr(&ctl->sfull[slot]));
+        } else {
+          if (!sched_take(slot, spar, u)) {
+            ok = false;
+            break;
+          }
+          sched_release(slot);
         }
-        int u = atomicAdd(L.counter, 1);
-        if (u >= total_units) u = -1;
-        ctl->sched[slot] = u;
-        mbar_arrive(smem_addr(&ctl->sfull[slot]));
         if (u < 0) break;
         int q;
         const int lu = split_unit(sc, u, q);
@@ -190,32 +259,51 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const bool a_mn = L.prob[q].a_mn != 0;
         int m, split, nb, ne;
         s.unit(lu, m, split, nb, ne);
+        const int arow = m * C::UNIT_M + static_cast<int>(rank) * BM;
         for (int n = nb; ok && n < ne; ++n) {
+          const int bcol = n * BN + static_cast<int>(rank) * C::B_ROWS;
           for (int kb = 0; kb < s.k_blocks; ++kb) {
-            const uint32_t fb = smem_addr(&ctl->full[stage]);
-            if (!wait_bounded(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
+            if (!wait_bounded<PAIR>(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t fb_local = smem_addr(&ctl->full[stage]);
+            if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * C::CTAS);
+            const uint32_t sa = smem_base + stage * C::STAGE;
             const uint32_t sb = sa + A_TILE_BYTES;
-            if (!a_mn) {
-              tma_load_2d(sa, ma, fb, kb * BK, m * BM);
-            } else {
-              tma_load_2d(sa, ma, fb, m * BM, kb * BK);
-              tma_load_2d(sa + 8192, ma, fb, m * BM + 64, kb * BK);
-            }
-            if (!B_MN) {
-              tma_load_2d(sb, mb, fb, kb * BK, n * BN);
-            } else {
+            if constexpr (PAIR) {
+              const uint32_t fb = map_to_cta(fb_local, 0);
+              if (!a_mn) {
+                tma_load_2d_pair(sa, ma, fb, kb * BK, arow);
+              } else {
+                tma_load_2d_pair(sa, ma, fb, arow, kb * BK);
+                tma_load_2d_pair(sa + 8192, ma, fb, arow + 64, kb * BK);
+              }
+              if (!B_MN) {
+                tma_load_2d_pair(sb, mb, fb, kb * BK, bcol);
+              } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(sb + j * 8192, mb, fb, n * BN + 64 * j, kb * BK);
+                for (int j = 0; j < C::B_ROWS / 64; ++j)
+                  tma_load_2d_pair(sb + j * 8192, mb, fb, bcol + 64 * j, kb * BK);
+              }
+            } else {
+              if (!a_mn) {
+                tma_load_2d(sa, ma, fb_local, kb * BK, arow);
+              } else {
+                tma_load_2d(sa, ma, fb_local, arow, kb * BK);
+                tma_load_2d(sa + 8192, ma, fb_local, arow + 64, kb * BK);
+              }
+              if (!B_MN) {
+                tma_load_2d(sb, mb, fb_local, kb * BK, bcol);
+              } else {
+#pragma unroll
+                for (int j = 0; j < C::B_ROWS / 64; ++j)
+                  tma_load_2d(sb + j * 8192, mb, fb_local, bcol + 64 * j, kb * BK);
+              }
             }
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) {
+            if (++stage == C::NSTAGE) {
               stage = 0;
               phase ^= 1;
             }
@@ -223,26 +311,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       }
       if (!ok) {
-        for (int s = 0; s < STAGES; ++s)
-          if (issued_mask & (1u << s)) wait_drain(smem_addr(&ctl->full[s]), (issued_par >> s) & 1);
+        if constexpr (PAIR) {
+          pause_ns(100000);   // let copies already issued land before exit
+        } else {
+          for (int s = 0; s < C::NSTAGE; ++s)
+            if (issued_mask & (1u << s))
+              wait_drain(smem_addr(&ctl->full[s]), (issued_par >> s) & 1);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_AK = idesc_bf16_f32(BM, BN, false, B_MN);
-      constexpr uint32_t IDESC_AMN = idesc_bf16_f32(BM, BN, true, B_MN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC_AK = idesc_bf16_f32(C::UNIT_M, BN, false, B_MN);
+      constexpr uint32_t IDESC_AMN = idesc_bf16_f32(C::UNIT_M, BN, true, B_MN);
+      constexpr uint32_t B_LBO = 8192;   // MN-major: the 64-wide N chunks are 8 KB apart
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int i = 0; ok; ++i) {
         const int slot = i & (SCHED_DEPTH - 1);
         const uint32_t spar = (i / SCHED_DEPTH) & 1;
-        if (!wait_bounded(smem_addr(&ctl->sfull[slot]), spar, abort, status)) {
+        int u;
+        if (!sched_take(slot, spar, u)) {
           ok = false;
           break;
         }
-        const int u = ctl->sched[slot];
-        mbar_arrive(smem_addr(&ctl->sempty[slot]));
+        sched_release(slot);
         if (u < 0) break;
         int q;
         const int lu = split_unit(sc, u, q);
@@ -253,19 +347,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         int m, split, nb, ne;
         s.unit(lu, m, split, nb, ne);
         for (int n = nb; ok && n < ne; ++n) {
-          if (!wait_bounded(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, status)) {
+          if (!wait_bounded<PAIR>(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + acc * BN;
           for (int kb = 0; kb < s.k_blocks; ++kb) {
-            if (!wait_bounded(smem_addr(&ctl->full[stage]), phase, abort, status)) {
+            if (!wait_bounded<PAIR>(smem_addr(&ctl->full[stage]), phase, abort, status)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const uint32_t sa = smem_base + stage * STAGE_BYTES;
+            const uint32_t sa = smem_base + stage * C::STAGE;
             const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
@@ -274,24 +368,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               // with the 64-wide MN chunks 8 KB apart.
               const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
-              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, B_LBO, 1024)
                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
-            umma_commit(smem_addr(&ctl->empty[stage]));
-            if (++stage == STAGES) {
+            if constexpr (PAIR)
+              umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+            else
+              umma_commit(smem_addr(&ctl->empty[stage]));
+            if (++stage == C::NSTAGE) {
               stage = 0;
               phase ^= 1;
             }
           }
           if (!ok) break;
-          umma_commit(smem_addr(&ctl->tfull[acc]));
+          if constexpr (PAIR)
+            umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
+          else
+            umma_commit(smem_addr(&ctl->tfull[acc]));
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1;
         }
       }
       if (!ok) {
-        umma_commit(smem_addr(&ctl->drain));
+        if constexpr (PAIR) {
+          umma_commit_pair(smem_addr(&ctl->drain), 0x1);
+        } else {
+          umma_commit(smem_addr(&ctl->drain));
+        }
         wait_drain(smem_addr(&ctl->drain), 0);
       }
     }
@@ -301,20 +408,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int lrow = qw * 32 + lane;    // accumulator row of this thread
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     uint32_t acc = 0, acc_phase = 0;
+    const uint32_t tempty_leader =
+        PAIR ? map_to_cta(smem_addr(&ctl->tempty[0]), 0) : smem_addr(&ctl->tempty[0]);
 
     for (int i = 0;; ++i) {
       const int slot = i & (SCHED_DEPTH - 1);
       const uint32_t spar = (i / SCHED_DEPTH) & 1;
       int u = 0;
       uint32_t got = 1;
-      if (lane == 0) {
-        got = wait_bounded(smem_addr(&ctl->sfull[slot]), spar, abort, status) ? 1u : 0u;
-        if (got) u = ctl->sched[slot];
-      }
+      if (lane == 0) got = sched_take(slot, spar, u) ? 1u : 0u;
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       u = __shfl_sync(0xffffffffu, u, 0);
-      if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[slot]));
+      if (lane == 0) sched_release(slot);
       if (u < 0) break;
       int q;
       const int lu = split_unit(sc, u, q);
@@ -322,7 +428,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const GemmArgs& p = L.prob[q].p;
       int m, split, nb, ne;
       s.unit(lu, m, split, nb, ne);
-      const int row = m * BM + lrow;
+      const int row = m * C::UNIT_M + static_cast<int>(rank) * BM + lrow;
 
       if (s.k_blocks == 0) {
         if constexpr (EPI == EPI_STORE_F32) {
@@ -362,7 +468,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int n = nb; n < ne; ++n) {
         uint32_t t_ok = 1;
         if (lane == 0)
-          t_ok = wait_bounded(smem_addr(&ctl->tfull[acc]), acc_phase, abort, status) ? 1u : 0u;
+          t_ok = wait_bounded<PAIR>(smem_addr(&ctl->tfull[acc]), acc_phase, abort, status) ? 1u : 0u;
         t_ok = __shfl_sync(0xffffffffu, t_ok, 0);
         if (!t_ok) {
           ok = false;
@@ -381,7 +487,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // the accumulator is fully read: hand it back to the MMA warp
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->tempty[acc]));
+            if (lane == 0) {
+              if constexpr (PAIR)
+                mbar_arrive_remote(tempty_leader + acc * sizeof(uint64_t));
+              else
+                mbar_arrive(smem_addr(&ctl->tempty[acc]));
+            }
           }
           const int cb = c * 32;
           const int lim = p.n_extent - col0 - cb;   // valid columns in this chunk
@@ -498,20 +609,71 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // no remote arrive may target an exited CTA
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-template <int EPI, bool B_MN>
+// Co-resident clusters of two for a kernel (cached per kernel and device).
+template <class K>
+int max_active_pairs(K kern) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  cache[dev] = n;
+  return n;
+}
+
+// grid = CTAs wanted (ignored beyond the co-resident limit).  For pairs the
+// grid is rounded to whole clusters.
+template <int EPI, bool B_MN, bool PAIR>
 cudaError_t launch_tc_gemm(const LaunchArgs& a, int grid, cudaStream_t s) {
-  auto kern = tc_gemm_kernel<EPI, B_MN>;
+  auto kern = tc_gemm_kernel<EPI, B_MN, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(GEMM_SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(a);
-  return cudaGetLastError();
+  if constexpr (!PAIR) {
+    kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(a);
+    return cudaGetLastError();
+  } else {
+    const int pairs_max = max_active_pairs(kern);
+    if (pairs_max <= 0) return cudaErrorInvalidConfiguration;
+    int pairs = (grid + 1) / 2;
+    if (pairs > pairs_max) pairs = pairs_max;
+    if (pairs < 1) pairs = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+  }
 }
 
 }  // namespace lmh
