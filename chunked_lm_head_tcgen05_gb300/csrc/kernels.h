@@ -21,7 +21,10 @@ constexpr uint32_t STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int EPI_WARPS = 4;
 constexpr int GEMM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators, double buffered
-constexpr size_t GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+// Epilogue staging: two 16 KB buffers (128 rows x 128 bytes, 128-byte
+// swizzled) that TMA bulk-stores write out.
+constexpr uint32_t STAGING_BYTES = 2 * 16384;
+constexpr size_t GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 256 + 1024;
 
 // Device status word values (same numbers as the public lmhead_status).
 constexpr int STATUS_DEVICE_TIMEOUT = 5;
@@ -67,6 +70,9 @@ struct GemmArgs {
   const int* row_map;    // EPI_STORE_F32: optional output row of row (row_base + r)
   int accumulate;        // EPI_STORE_F32: 1 = add to the existing values
   int zero_if_empty;     // EPI_STORE_F32: K == 0 and !accumulate writes zeros
+  int n_fastest;         // unit order: 1 = N tiles of one M block consecutively (one tile per unit)
+  int out_mode;          // 0: per-thread global stores; 1: TMA store of map_out tiles;
+                         // 2: TMA reduce-add into map_out (EPI_STORE_F32 accumulation)
 };
 
 // One launch of the tensor-core GEMM runs one or two problems (GEMMs with
@@ -84,6 +90,7 @@ struct Problem {
 struct LaunchArgs {
   CUtensorMap map_a[MAX_PROBLEMS];
   CUtensorMap map_b[MAX_PROBLEMS];
+  CUtensorMap map_out[MAX_PROBLEMS];   // output tiles for out_mode 1 / 2 (box 128 rows x 128 bytes)
   Problem prob[MAX_PROBLEMS];
   int n_problems;
   int* counter;

@@ -113,18 +113,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 map: `inner` contiguous elements per row, `outer` rows, rows
 // `row_bytes` apart; boxes of box_inner x box_outer with 128-byte swizzle.
 // Elements outside the map read as zero.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-              uint32_t box_inner, uint32_t box_outer) {
+bool make_map_typed(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
   auto enc = encode_fn();
   if (!enc || inner == 0 || outer == 0) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, type, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer) {
+  return make_map_typed(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes,
+                        box_inner, box_outer);
+}
+
+// fp32 output map with 128-row x 32-column (128-byte) boxes for staged
+// epilogue stores and reduce-adds.
+bool make_out_map_f32(CUtensorMap* m, const float* base, uint64_t cols, uint64_t rows,
+                      uint64_t ld) {
+  return make_map_typed(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, cols, rows, 4 * ld, 32, BM);
 }
 
 // ------------------------------------------------------------------ plans
@@ -465,6 +477,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       pz.coef = coef;
       pz.dz_out = dz;
       pz.dz_ld = static_cast<int>(bp.Vb);
+      pz.out_mode = 1;
+      if (!make_map(&lz.map_out[0], dz, vact, m_cap, 2ull * bp.Vb, 64, BM)) return LMHEAD_ERR_CUDA;
       lz.n_problems = 1;
       lz.counter = counter;
       const int gz = static_cast<int>(
@@ -491,6 +505,14 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       ph.out_ld = H;
       ph.row_map = f.idx;
       ph.accumulate = vb > 0 ? 1 : 0;
+      ph.n_fastest = 1;
+      if (!f.idx) {
+        // every token scored: compacted rows are the rows of d_hidden
+        ph.out_mode = ph.accumulate ? 2 : 1;
+        if (!make_out_map_f32(&lg.map_out[0], d_hidden + t0 * H, H,
+                              std::min<int64_t>(m_cap, T - t0), H))
+          return LMHEAD_ERR_CUDA;
+      }
       // problem 1: dW[block vocab rows] (+)= dz^T . h_block (K = tokens, ascending blocks)
       if (!make_map(&lg.map_a[1], dz, vact, m_cap, 2ull * bp.Vb, 64, 64)) return LMHEAD_ERR_CUDA;
       if (!make_map(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
@@ -508,6 +530,9 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       pw.out_ld = H;
       pw.accumulate = (tb > 0 || accumulate_dweight) ? 1 : 0;
       pw.zero_if_empty = 1;
+      pw.n_fastest = 1;
+      pw.out_mode = pw.accumulate ? 2 : 1;
+      if (!make_out_map_f32(&lg.map_out[1], d_weight + v0 * H, H, vact, H)) return LMHEAD_ERR_CUDA;
       lg.n_problems = 2;
       lg.counter = counter + 1;
       const int gg = static_cast<int>(std::min<int64_t>(

@@ -40,6 +40,8 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#include <climits>
+
 namespace lmh {
 
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -69,6 +71,8 @@ struct SharedCtl {
   int sched[SCHED_DEPTH];
   uint32_t tmem_base;
   int abort;
+  int epi_u;    // unit index broadcast to the epilogue warps
+  int epi_ok;   // accumulator-ready flag broadcast to the epilogue warps
 };
 static_assert(sizeof(SharedCtl) <= 256, "control block exceeds its shared memory slot");
 
@@ -111,7 +115,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 }
 
 struct Sched {
-  int M, K, m_tiles, n_tiles, n_splits, k_blocks, units;
+  int M, K, m_tiles, n_tiles, n_splits, k_blocks, units, n_fastest;
 
   __device__ __forceinline__ void init(const GemmArgs& p, int unit_m) {
     int dev = 0;
@@ -124,24 +128,58 @@ struct Sched {
     n_splits = p.n_splits > 0 ? min(p.n_splits, n_tiles) : n_tiles;
     k_blocks = (K + BK - 1) / BK;
     units = m_tiles * n_splits;
+    n_fastest = p.n_fastest && n_splits == n_tiles;
   }
 
+  // Unit u -> M block m and N tiles [nb, ne).  M-fastest order lets units
+  // that run together share the B panel; N-fastest lets them share A.
   __device__ __forceinline__ void unit(int u, int& m, int& split, int& nb, int& ne) const {
-    m = u % m_tiles;
-    split = u / m_tiles;
+    if (n_fastest) {
+      m = u / n_splits;
+      split = u - m * n_splits;
+    } else {
+      m = u % m_tiles;
+      split = u / m_tiles;
+    }
     nb = static_cast<int>(static_cast<long long>(split) * n_tiles / n_splits);
     ne = static_cast<int>(static_cast<long long>(split + 1) * n_tiles / n_splits);
   }
 };
 
 // Global unit index -> (problem, unit within it).
-__device__ __forceinline__ int split_unit(const Sched* sc, int u, int& q) {
-  if (u < sc[0].units) {
+__device__ __forceinline__ int split_unit(const Sched& s0, int u, int& q) {
+  if (u < s0.units) {
     q = 0;
     return u;
   }
   q = 1;
-  return u - sc[0].units;
+  return u - s0.units;
+}
+
+// Write one thread's 128-byte row piece (8 x 16 bytes) into staging buffer
+// (nstore & 1) in the 128-byte swizzled layout and hand the 128-row tile to
+// TMA (store, or reduce-add for mode 2).  All 128 epilogue threads call it
+// together; `issuer` is the one thread that drives TMA.
+__device__ __forceinline__ void stage_out(const uint32_t* w, uint32_t stg0, uint32_t nstore,
+                                          int lrow, bool issuer, const CUtensorMap* map, int mode,
+                                          int x, int y) {
+  const uint32_t buf = stg0 + (nstore & 1u) * 16384u;
+  if (issuer && nstore >= 2) bulk_wait_read<1>();
+  named_bar_sync(1, 128);
+  const uint32_t rowb = buf + static_cast<uint32_t>(lrow) * 128u;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    st_shared_v4(rowb + ((static_cast<uint32_t>(c) ^ (static_cast<uint32_t>(lrow) & 7u)) << 4),
+                 w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  fence_async_smem();
+  named_bar_sync(1, 128);
+  if (issuer) {
+    if (mode == 2)
+      tma_reduce_add_2d(map, buf, x, y);
+    else
+      tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
 }
 
 template <int EPI, bool B_MN, bool PAIR>
@@ -151,22 +189,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int* const status = L.prob[0].p.status;
   const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
   const bool leader = rank == 0;
 
-  Sched sc[MAX_PROBLEMS];
-  sc[0].init(L.prob[0].p, C::UNIT_M);
+  Sched sc0, sc1;
+  sc0.init(L.prob[0].p, C::UNIT_M);
   if (L.n_problems > 1) {
-    sc[1].init(L.prob[1].p, C::UNIT_M);
+    sc1.init(L.prob[1].p, C::UNIT_M);
   } else {
-    sc[1] = sc[0];
-    sc[1].units = 0;
+    sc1 = sc0;
+    sc1.units = 0;
   }
-  const int total_units = sc[0].units + sc[1].units;
+  const int total_units = sc0.units + sc1.units;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -179,7 +217,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int s = 0; s < SCHED_DEPTH; ++s) {
       mbar_init(smem_addr(&ctl->sfull[s]), 1);
-      mbar_init(smem_addr(&ctl->sempty[s]), (1 + EPI_WARPS) * C::CTAS);
+      mbar_init(smem_addr(&ctl->sempty[s]), 2 * C::CTAS);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
@@ -251,8 +289,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         if (u < 0) break;
         int q;
-        const int lu = split_unit(sc, u, q);
-        const Sched& s = sc[q];
+        const int lu = split_unit(sc0, u, q);
+        const Sched s = q ? sc1 : sc0;
         if (s.k_blocks == 0) continue;
         const CUtensorMap* ma = &L.map_a[q];
         const CUtensorMap* mb = &L.map_b[q];
@@ -339,8 +377,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         sched_release(slot);
         if (u < 0) break;
         int q;
-        const int lu = split_unit(sc, u, q);
-        const Sched& s = sc[q];
+        const int lu = split_unit(sc0, u, q);
+        const Sched s = q ? sc1 : sc0;
         if (s.k_blocks == 0) continue;
         const bool a_mn = L.prob[q].a_mn != 0;
         const uint32_t idesc = a_mn ? IDESC_AMN : IDESC_AK;
@@ -404,31 +442,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Decisions that all four epilogue warps must take together (the next
+    // unit, whether an accumulator is ready) are made by one issuer thread
+    // and broadcast through shared memory between named barriers, so the
+    // warps can never part ways at a barrier.
     const int qw = warp & 3;            // TMEM lane quarter this warp may read
     const int lrow = qw * 32 + lane;    // accumulator row of this thread
+    const bool issuer = lrow == 0;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t stg0 = smem_base + STAGES * STAGE_BYTES;
     uint32_t acc = 0, acc_phase = 0;
+    uint32_t nstore = 0;   // staged TMA stores issued so far (buffer parity)
     const uint32_t tempty_leader =
         PAIR ? map_to_cta(smem_addr(&ctl->tempty[0]), 0) : smem_addr(&ctl->tempty[0]);
+    volatile int* epi_u = &ctl->epi_u;
+    volatile int* epi_ok = &ctl->epi_ok;
 
     for (int i = 0;; ++i) {
       const int slot = i & (SCHED_DEPTH - 1);
       const uint32_t spar = (i / SCHED_DEPTH) & 1;
-      int u = 0;
-      uint32_t got = 1;
-      if (lane == 0) got = sched_take(slot, spar, u) ? 1u : 0u;
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) break;
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (lane == 0) sched_release(slot);
-      if (u < 0) break;
+      if (issuer) {
+        int uu = 0;
+        const bool got = sched_take(slot, spar, uu);
+        if (got) sched_release(slot);
+        *epi_u = got ? uu : INT_MIN;
+      }
+      named_bar_sync(1, 128);
+      const int u = *epi_u;
+      named_bar_sync(1, 128);
+      if (u < 0) break;   // no more work, or the scheduler gave up
       int q;
-      const int lu = split_unit(sc, u, q);
-      const Sched& s = sc[q];
+      const int lu = split_unit(sc0, u, q);
+      const Sched s = q ? sc1 : sc0;
       const GemmArgs& p = L.prob[q].p;
+      const CUtensorMap* map_out = &L.map_out[q];
       int m, split, nb, ne;
       s.unit(lu, m, split, nb, ne);
-      const int row = m * C::UNIT_M + static_cast<int>(rank) * BM + lrow;
+      const int row_t = m * C::UNIT_M + static_cast<int>(rank) * BM;   // first row of this CTA's tile
+      const int row = row_t + lrow;
 
       if (s.k_blocks == 0) {
         if constexpr (EPI == EPI_STORE_F32) {
@@ -461,15 +512,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
       } else {
         row_ok = row < s.M;
-        if (row_ok) orow = p.row_map ? p.row_map[p.row_base + row] : p.row_base + row;
+        if (row_ok && p.out_mode == 0)
+          orow = p.row_map ? p.row_map[p.row_base + row] : p.row_base + row;
       }
 
       bool ok = true;
       for (int n = nb; n < ne; ++n) {
-        uint32_t t_ok = 1;
-        if (lane == 0)
-          t_ok = wait_bounded<PAIR>(smem_addr(&ctl->tfull[acc]), acc_phase, abort, status) ? 1u : 0u;
-        t_ok = __shfl_sync(0xffffffffu, t_ok, 0);
+        if (issuer)
+          *epi_ok = wait_bounded<PAIR>(smem_addr(&ctl->tfull[acc]), acc_phase, abort, status) ? 1 : 0;
+        named_bar_sync(1, 128);
+        const int t_ok = *epi_ok;
+        named_bar_sync(1, 128);
         if (!t_ok) {
           ok = false;
           break;
@@ -478,26 +531,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int col0 = n * BN;
         const uint32_t tcol = tmem_base + lane_off + acc * BN;
         const int yt = y - p.col_base - col0;
-
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_load_32(tcol + c * 32, v);
-          if (c == BN / 32 - 1) {
-            // the accumulator is fully read: hand it back to the MMA warp
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (PAIR)
-                mbar_arrive_remote(tempty_leader + acc * sizeof(uint64_t));
-              else
-                mbar_arrive(smem_addr(&ctl->tempty[acc]));
-            }
+        // hand the accumulator back to the MMA warp once this warp has read it all
+        auto release_acc = [&]() {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (PAIR)
+              mbar_arrive_remote(tempty_leader + acc * sizeof(uint64_t));
+            else
+              mbar_arrive(smem_addr(&ctl->tempty[acc]));
           }
-          const int cb = c * 32;
-          const int lim = p.n_extent - col0 - cb;   // valid columns in this chunk
+        };
 
-          if constexpr (EPI == EPI_FWD_STATS) {
+        if constexpr (EPI == EPI_FWD_STATS) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load_32(tcol + c * 32, v);
+            if (c == BN / 32 - 1) release_acc();
+            const int cb = c * 32;
+            const int lim = p.n_extent - col0 - cb;   // valid columns in this chunk
             float cmax = -INFINITY;
             if (lim >= 32) {
 #pragma unroll
@@ -539,39 +592,66 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < 32; ++j)
                 if (j == yt - cb) zy = v[j] * p.scale;
             }
-          } else if constexpr (EPI == EPI_BWD_DZ) {
-            float g[32];
+          }
+        } else if constexpr (EPI == EPI_BWD_DZ) {
+          // 64 columns per staged chunk: 128 bytes of bf16 per row
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 64; ++cc) {
+            uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = fmaf(v[j], p.scale, -cf.x);
-              const float pr = ex2_approx(d);
-              g[j] = -pr * fmaf(cf.y, d, cf.z);
+            for (int h = 0; h < 2; ++h) {
+              float v[32];
+              tmem_load_32(tcol + cc * 64 + h * 32, v);
+              if (cc == BN / 64 - 1 && h == 1) release_acc();
+              const int cb = cc * 64 + h * 32;
+              float g[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float d = fmaf(v[j], p.scale, -cf.x);
+                const float pr = ex2_approx(d);
+                g[j] = -pr * fmaf(cf.y, d, cf.z);
+              }
+              if (static_cast<unsigned>(yt - cb) < 32u) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j == yt - cb) g[j] += cf.w;
+              }
+#pragma unroll
+              for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
             }
-            if (static_cast<unsigned>(yt - cb) < 32u) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j == yt - cb) g[j] += cf.w;
-            }
-            if (row_ok && lim > 0) {
-              uint16_t* dst = p.dz_out + static_cast<int64_t>(row) * p.dz_ld + col0 + cb;
-              uint32_t pk[16];
-#pragma unroll
-              for (int k = 0; k < 16; ++k) pk[k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
-              if (lim >= 32) {
+            if (p.out_mode == 1) {
+              stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t);
+            } else if (row_ok) {
+              const int lim = p.n_extent - col0 - cc * 64;
+              uint16_t* dst = p.dz_out + static_cast<int64_t>(row) * p.dz_ld + col0 + cc * 64;
+              if (lim >= 64) {
                 uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
+                for (int k = 0; k < 8; ++k)
                   d4[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
               } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < 64; ++j)
                   if (j < lim)
                     dst[j] = static_cast<uint16_t>((j & 1) ? (pk[j >> 1] >> 16)
                                                            : (pk[j >> 1] & 0xFFFFu));
               }
             }
-          } else {
-            if (row_ok && lim > 0) {
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load_32(tcol + c * 32, v);
+            if (c == BN / 32 - 1) release_acc();
+            const int cb = c * 32;
+            if (p.out_mode != 0) {
+              uint32_t w[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
+              stage_out(w, stg0, nstore++, lrow, issuer, map_out, p.out_mode, col0 + cb, row_t);
+            } else if (row_ok) {
+              const int lim = p.n_extent - col0 - cb;
               float* dst = p.out + orow * p.out_ld + col0 + cb;
               if (lim >= 32) {
                 float4* d4 = reinterpret_cast<float4*>(dst);
@@ -605,6 +685,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               make_float4(mrun, ssum, s1, zy);
       }
     }
+    if (issuer) bulk_wait_all();   // staged stores done before the staging memory goes away
   }
 
   tc_fence_before_sync();
