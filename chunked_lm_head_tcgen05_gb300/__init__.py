@@ -20,11 +20,17 @@ __all__ = [
     "lmhead_read_device_status", "lmhead_read_scored_count", "lmhead_status_string",
     "lmhead_plan_info", "lmhead_profile_enable", "lmhead_profile_count",
     "lmhead_profile_record", "lmhead_launch_count", "lmhead_logps_fwd_noalloc",
-    "NOALLOC_SCRATCH_BYTES", "forward", "backward",
+    "NOALLOC_SCRATCH_BYTES", "lmhead_logps_fwd_bwd", "lmhead_fwd_bwd_keeps_logits",
+    "LMHEAD_OP_FWD_BWD", "LMHEAD_STRATEGY_AUTO", "LMHEAD_STRATEGY_RECOMPUTE",
+    "LMHEAD_STRATEGY_KEEP_LOGITS", "forward", "backward",
 ]
 
 LMHEAD_OP_FWD = 0
 LMHEAD_OP_BWD = 1
+LMHEAD_OP_FWD_BWD = 2
+LMHEAD_STRATEGY_AUTO = 0
+LMHEAD_STRATEGY_RECOMPUTE = 1
+LMHEAD_STRATEGY_KEEP_LOGITS = 2
 NOALLOC_SCRATCH_BYTES = 64 << 20   # LMHEAD_NOALLOC_SCRATCH_BYTES in include/lmhead.h
 STATUS_NAMES = {
     0: "LMHEAD_OK", 1: "LMHEAD_ERR_INVALID_ARG", 2: "LMHEAD_ERR_UNSUPPORTED",
@@ -61,6 +67,11 @@ _SIGNATURES = {
     "lmhead_launch_count": (ctypes.c_uint64, []),
     "lmhead_logps_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32,
                                                 ctypes.c_float, _I32, _VP, _VP, _VP, _VP]),
+    "lmhead_logps_fwd_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32,
+                                            ctypes.c_float, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            _VP, ctypes.c_int, ctypes.c_int, _VP, _SZ, _VP]),
+    "lmhead_fwd_bwd_keeps_logits": (ctypes.c_int, [_I64, _I32, _I32, _I32,
+                                                   ctypes.POINTER(_I32)]),
 }
 
 
@@ -189,6 +200,40 @@ def lmhead_logps_fwd_noalloc(hidden, weight, targets, loss_mask, temperature, ch
     return int(library().lmhead_logps_fwd_noalloc(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
         int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _stream(stream)))
+
+
+def lmhead_logps_fwd_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
+                         grad_entropy, logp, entropy, lse, d_hidden, d_weight,
+                         accumulate_dweight, strategy, workspace, stream=None):
+    """C ``lmhead_logps_fwd_bwd`` on torch tensors; returns the status code."""
+    import torch
+    T, H = hidden.shape
+    V = weight.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight, "weight", torch.bfloat16, (V, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(grad_logp, "grad_logp", torch.float32, (T,), allow_none=True)
+    _check_tensor(grad_entropy, "grad_entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(logp, "logp", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    _check_tensor(d_hidden, "d_hidden", torch.float32, (T, H))
+    _check_tensor(d_weight, "d_weight", torch.float32, (V, H))
+    return int(library().lmhead_logps_fwd_bwd(
+        _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
+        int(chunk_size), _ptr(grad_logp), _ptr(grad_entropy), _ptr(logp), _ptr(entropy),
+        _ptr(lse), _ptr(d_hidden), _ptr(d_weight), int(bool(accumulate_dweight)), int(strategy),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lmhead_fwd_bwd_keeps_logits(T, H, V, chunk_size):
+    """(keeps logits under AUTO: bool, token block of the keep-logits path)."""
+    tb = _I32()
+    r = int(library().lmhead_fwd_bwd_keeps_logits(T, H, V, chunk_size, ctypes.byref(tb)))
+    if r < 0:
+        raise LmheadError(1, "lmhead_fwd_bwd_keeps_logits")
+    return bool(r), tb.value
 
 
 def lmhead_read_device_status(workspace, stream=None):

@@ -4,6 +4,9 @@
 // coefficients and the zeroing of unscored rows.
 #include "kernels.h"
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 namespace lmh {
@@ -117,9 +120,10 @@ __global__ void zero_masked_outputs_kernel(const uint8_t* __restrict__ mask, int
 // deterministic.
 __global__ void fwd_merge_kernel(const float4* __restrict__ part, int n_splits, int part_ld,
                                  const int* __restrict__ idx, const int* __restrict__ y_c,
-                                 const DeviceState* st, float* logp, float* entropy, float* lse) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= st->rows) return;
+                                 const DeviceState* st, int r0, int r1, float* logp,
+                                 float* entropy, float* lse) {
+  const int r = r0 + blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= r1 || r >= st->rows) return;
   float M = -INFINITY;
   for (int j = 0; j < n_splits; ++j) M = fmaxf(M, part[static_cast<int64_t>(j) * part_ld + r].x);
   float s = 0.f, s1 = 0.f, zy = -INFINITY;
@@ -141,13 +145,13 @@ __global__ void fwd_merge_kernel(const float4* __restrict__ part, int n_splits, 
 // Per scored row: {lse * log2 e, g_e ln2 / tau, (g_l + g_e H) / tau, g_l / tau}
 // so that dz / tau = -p (a d + b) + c [v == y], with d = log2 p.  Rows past
 // the scored count get zeros (their dz is then exactly zero).
-__global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* st, int T_alloc,
+__global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* st, int r0, int r1,
                                 const float* __restrict__ lse, const float* __restrict__ entropy,
                                 const float* __restrict__ grad_logp,
                                 const float* __restrict__ grad_entropy, float inv_tau,
                                 float4* __restrict__ coef) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= T_alloc) return;
+  const int r = r0 + blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= r1) return;
   float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
   if (r < st->rows) {
     const int t = idx ? idx[r] : r;
@@ -169,6 +173,57 @@ __global__ void zero_masked_rows_kernel(const uint8_t* __restrict__ mask, int T,
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / H4);
     if (!mask[t]) d_hidden[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// In-place logits -> dz for a token block of the single-call path.  Element
+// (r, c): u - m' is stored as fp16 with m' = m_tile[r][c / 256]; with
+// d = u - lse_u = log2 p:  dz / tau = -p (a d + b) + c1 [c == y]  (the
+// per-row coefficients of bwd_prep_kernel), written back as bf16.  Rows
+// past the scored count have zero coefficients and become exact zeros.
+__global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* __restrict__ m_tile,
+                                int mt_ld, const float4* __restrict__ coef,
+                                const int* __restrict__ y_c, const DeviceState* st, int t0,
+                                int rows_cap, int V) {
+  int dyn = st->rows - t0;
+  dyn = dyn < 0 ? 0 : (dyn > rows_cap ? rows_cap : dyn);
+  // rows the gradient GEMMs read: whole 128-row tiles (zero padding rows included)
+  const int rows = min(rows_cap, (dyn + BM - 1) / BM * BM);
+  const int groups = (V + 7) / 8;
+  const int64_t n = static_cast<int64_t>(rows) * groups;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / groups);
+    const int c0 = static_cast<int>(i - static_cast<int64_t>(r) * groups) * 8;
+    const float4 cf = coef[t0 + r];
+    const int y = y_c[t0 + r];
+    const float base = m_tile[static_cast<int64_t>(r) * mt_ld + c0 / BN] - cf.x;
+    uint16_t* row = z + static_cast<int64_t>(r) * ld + c0;
+    const uint4 raw = *reinterpret_cast<const uint4*>(row);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+      float g[2];
+      const float uu[2] = {u.x, u.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float d = uu[e] + base;
+        const float pr = exp2f(d);
+        g[e] = -pr * fmaf(cf.y, d, cf.z);
+        if (c0 + 2 * k + e == y) g[e] += cf.w;
+      }
+      const __nv_bfloat162 b = __floats2bfloat162_rn(g[0], g[1]);
+      out[k] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    if (c0 + 8 <= V) {
+      *reinterpret_cast<uint4*>(row) = make_uint4(out[0], out[1], out[2], out[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < V) row[j] = static_cast<uint16_t>((j & 1) ? (out[j >> 1] >> 16) : (out[j >> 1] & 0xFFFFu));
+    }
   }
 }
 
@@ -212,18 +267,29 @@ cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, 
 }
 
 cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
-                             const int* y_c, const DeviceState* st, int T_alloc, float* logp,
+                             const int* y_c, const DeviceState* st, int r0, int r1, float* logp,
                              float* entropy, float* lse, cudaStream_t s) {
-  fwd_merge_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(partials, n_splits, part_ld, idx, y_c, st,
-                                                          logp, entropy, lse);
+  if (r1 <= r0) return cudaSuccess;
+  fwd_merge_kernel<<<(r1 - r0 + 255) / 256, 256, 0, s>>>(partials, n_splits, part_ld, idx, y_c,
+                                                          st, r0, r1, logp, entropy, lse);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int T_alloc, const float* lse,
+cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r1, const float* lse,
                             const float* entropy, const float* grad_logp,
                             const float* grad_entropy, float tau, float4* coef, cudaStream_t s) {
-  bwd_prep_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(idx, st, T_alloc, lse, entropy, grad_logp,
+  if (r1 <= r0) return cudaSuccess;
+  bwd_prep_kernel<<<(r1 - r0 + 255) / 256, 256, 0, s>>>(idx, st, r0, r1, lse, entropy, grad_logp,
                                                          grad_entropy, 1.0f / tau, coef);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_tile_ld,
+                            const float4* coef, const int* y_c, const DeviceState* st, int t0,
+                            int rows_cap, int V, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(rows_cap) * ((V + 7) / 8);
+  fused_dz_kernel<<<grid_for(n, 256, 152 * 16), 256, 0, s>>>(z16, ld, m_tile, m_tile_ld, coef, y_c,
+                                                             st, t0, rows_cap, V);
   return cudaGetLastError();
 }
 

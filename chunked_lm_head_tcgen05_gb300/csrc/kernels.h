@@ -41,6 +41,8 @@ enum EpiKind : int {
   EPI_FWD_STATS = 0,   // online max / exp-sum / sum p*z / target logit per vocab split
   EPI_BWD_DZ = 1,      // dz = g_l (onehot - p) - g_e p (log p + H), divided by tau, to bf16
   EPI_STORE_F32 = 2,   // plain fp32 tile store or read-modify-write (dh, dW)
+  EPI_FWD_Z = 3,       // EPI_FWD_STATS, and also keep the logits: fp16 (u - m_tile) tiles
+                       // through map_out plus the per-(row, tile) reference m_tile
 };
 
 struct GemmArgs {
@@ -70,6 +72,8 @@ struct GemmArgs {
   const int* row_map;    // EPI_STORE_F32: optional output row of row (row_base + r)
   int accumulate;        // EPI_STORE_F32: 1 = add to the existing values
   int zero_if_empty;     // EPI_STORE_F32: K == 0 and !accumulate writes zeros
+  float* m_tile;         // EPI_FWD_Z: [rows][m_tile_ld] reference max of each 256-column tile
+  int m_tile_ld;
   int n_fastest;         // unit order: 1 = N tiles of one M block consecutively (one tile per unit)
   int out_mode;          // 0: per-thread global stores; 1: TMA store of map_out tiles;
                          // 2: TMA reduce-add into map_out (EPI_STORE_F32 accumulation)
@@ -103,6 +107,7 @@ struct LaunchArgs {
 cudaError_t launch_gemm_fwd_stats(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
 cudaError_t launch_gemm_bwd_dz(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
 cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
+cudaError_t launch_gemm_fwd_z(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
 
 // Auxiliary kernels (aux.cu).
 cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
@@ -113,12 +118,20 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, in
                                const DeviceState* st, uint16_t* h_c, cudaStream_t s);
 cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
                                        float* lse, cudaStream_t s);
+// Rows [r0, r1) of the compacted order (clipped to the scored count).
 cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
-                             const int* y_c, const DeviceState* st, int T_alloc, float* logp,
+                             const int* y_c, const DeviceState* st, int r0, int r1, float* logp,
                              float* entropy, float* lse, cudaStream_t s);
-cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int T_alloc, const float* lse,
+// Rows [r0, r1): coefficients of scored rows, zeros past the scored count.
+cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r1, const float* lse,
                             const float* entropy, const float* grad_logp,
                             const float* grad_entropy, float tau, float4* coef, cudaStream_t s);
+// In-place logits -> dz pass over a token block of the single-call path:
+// z16 holds fp16 (u - m_tile) for rows [0, rows_cap) of the block and
+// columns [0, V); it becomes bf16 dz / tau.
+cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_tile_ld,
+                            const float4* coef, const int* y_c, const DeviceState* st, int t0,
+                            int rows_cap, int V, cudaStream_t s);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
                                     cudaStream_t s);
 cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s);

@@ -132,6 +132,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
                         box_inner, box_outer);
 }
 
+bool make_map_f16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_map_typed(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, inner, outer, row_bytes,
+                        box_inner, box_outer);
+}
+
 // fp32 output map with 128-row x 32-column (128-byte) boxes for staged
 // epilogue stores and reduce-adds.
 bool make_out_map_f32(CUtensorMap* m, const float* base, uint64_t cols, uint64_t rows,
@@ -203,8 +209,41 @@ BwdPlan plan_bwd(int64_t T, int64_t V, int64_t chunk) {
   return p;
 }
 
+// Single-call forward + backward that keeps each token block's logits over
+// the whole vocabulary (T_b x V_pad 16-bit values <= chunk_size x V) instead
+// of recomputing them.  It pays when the recompute GEMM (2 T H V flops)
+// costs more than what keeping the logits adds: writing and re-reading them
+// (about 4 T V bytes) and the extra fp32 read-modify-write passes over dW
+// that the smaller token blocks cause (8 V H bytes each).
+struct FusedPlan {
+  int64_t Tb, n_tb, V_pad, n_tiles;
+  bool preferred;
+};
+
+FusedPlan plan_fused(int64_t T, int64_t H, int64_t V, int64_t chunk) {
+  FusedPlan p;
+  const int64_t T_alloc = round_up(T, BM);
+  p.V_pad = round_up(V, BN);
+  p.n_tiles = p.V_pad / BN;
+  const int64_t unit = 2 * BM;
+  int64_t tb = static_cast<int64_t>(static_cast<double>(chunk) * static_cast<double>(V) /
+                                    static_cast<double>(p.V_pad)) / unit * unit;
+  tb = std::max<int64_t>(unit, std::min<int64_t>(tb, round_up(T_alloc, unit)));
+  p.Tb = tb;
+  p.n_tb = ceil_div(T_alloc, tb);
+  const BwdPlan bp = plan_bwd(T, V, chunk);
+  const double flops_rate = 1.6e15, bytes_rate = 5.0e12;   // GB300 sustained, rounded down
+  const double TVd = static_cast<double>(T) * static_cast<double>(V);
+  const double dw_pass = 8.0 * static_cast<double>(V) * static_cast<double>(H) / bytes_rate;
+  const double split_cost = 2.0 * TVd * static_cast<double>(H) / flops_rate +
+                            static_cast<double>(bp.n_tb) * dw_pass;
+  const double fused_cost = 4.0 * TVd / bytes_rate + static_cast<double>(p.n_tb) * dw_pass;
+  p.preferred = fused_cost < split_cost;
+  return p;
+}
+
 struct Layout {
-  size_t state, counters, idx, y_c, h_c, part, coef, dz, total;
+  size_t state, counters, idx, y_c, h_c, part, coef, dz, m_tile, total;
   int64_t n_counters;   // dynamic work-unit counters, one per GEMM launch
 };
 
@@ -220,9 +259,11 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
   L.state = take(sizeof(DeviceState));
   if (op == LMHEAD_OP_FWD) {
     L.n_counters = 1;
-  } else {
+  } else if (op == LMHEAD_OP_BWD) {
     const BwdPlan bp = plan_bwd(T, V, chunk);
     L.n_counters = 2 * bp.n_tb * bp.n_vb;
+  } else {
+    L.n_counters = 2 * plan_fused(T, H, V, chunk).n_tb;
   }
   L.counters = take(4 * static_cast<size_t>(L.n_counters));
   L.idx = take(4 * static_cast<size_t>(T_alloc));
@@ -230,10 +271,16 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
   L.h_c = take(2 * static_cast<size_t>(T_alloc) * static_cast<size_t>(H));
   if (op == LMHEAD_OP_FWD) {
     L.part = take(16 * static_cast<size_t>(kMaxSplits) * static_cast<size_t>(T_alloc));
-  } else {
+  } else if (op == LMHEAD_OP_BWD) {
     const BwdPlan bp = plan_bwd(T, V, chunk);
     L.coef = take(16 * static_cast<size_t>(T_alloc));
     L.dz = take(2 * static_cast<size_t>(bp.Tb) * static_cast<size_t>(bp.Vb));
+  } else {
+    const FusedPlan fp = plan_fused(T, H, V, chunk);
+    L.part = take(16 * static_cast<size_t>(kMaxSplits) * static_cast<size_t>(T_alloc));
+    L.coef = take(16 * static_cast<size_t>(T_alloc));
+    L.dz = take(2 * static_cast<size_t>(fp.Tb) * static_cast<size_t>(fp.V_pad));
+    L.m_tile = take(4 * static_cast<size_t>(fp.Tb) * static_cast<size_t>(fp.n_tiles));
   }
   L.total = off;
   return L;
@@ -302,9 +349,13 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
 extern "C" {
 
 size_t lmhead_workspace_size(int op, int64_t T, int32_t H, int32_t V, int32_t chunk_size) {
-  if ((op != LMHEAD_OP_FWD && op != LMHEAD_OP_BWD) ||
+  if ((op != LMHEAD_OP_FWD && op != LMHEAD_OP_BWD && op != LMHEAD_OP_FWD_BWD) ||
       check_sizes(T, H, V, 1.0f, chunk_size) != LMHEAD_OK)
     return 0;
+  if (op == LMHEAD_OP_FWD_BWD)
+    return std::max({layout(LMHEAD_OP_FWD, T, H, V, chunk_size).total,
+                     layout(LMHEAD_OP_BWD, T, H, V, chunk_size).total,
+                     layout(LMHEAD_OP_FWD_BWD, T, H, V, chunk_size).total});
   return layout(op, T, H, V, chunk_size).total;
 }
 
@@ -384,7 +435,7 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   const int grid = static_cast<int>(std::min<int64_t>(m_tiles * splits * (pair ? 2 : 1), sms));
   LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(la, grid, pair, s); }));
   LMH_TRY(launch("fwd_merge", s, [&] {
-    return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st,
+    return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st, 0,
                             static_cast<int>(f.T_alloc), logp, entropy, lse, s);
   }));
   if (loss_mask) {
@@ -430,7 +481,7 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   float4* coef = reinterpret_cast<float4*>(ws + L.coef);
   uint16_t* dz = reinterpret_cast<uint16_t*>(ws + L.dz);
   LMH_TRY(launch("bwd_prep", s, [&] {
-    return launch_bwd_prep(f.idx, f.st, static_cast<int>(f.T_alloc), lse, entropy, grad_logp,
+    return launch_bwd_prep(f.idx, f.st, 0, static_cast<int>(f.T_alloc), lse, entropy, grad_logp,
                            grad_entropy, temperature, coef, s);
   }));
   if (loss_mask) {
@@ -543,6 +594,179 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   return LMHEAD_OK;
 }
 
+
+lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weight,
+                                   const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                                   int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                                   const float* grad_logp, const float* grad_entropy,
+                                   float* logp, float* entropy, float* lse, float* d_hidden,
+                                   float* d_weight, int accumulate_dweight, int strategy,
+                                   void* workspace, size_t workspace_bytes,
+                                   lmhead_stream_t stream) {
+  lmhead_status rc = check_sizes(T, H, V, temperature, chunk_size);
+  if (rc != LMHEAD_OK) return rc;
+  if (strategy < LMHEAD_STRATEGY_AUTO || strategy > LMHEAD_STRATEGY_KEEP_LOGITS)
+    return LMHEAD_ERR_INVALID_ARG;
+  if (!weight || !d_weight) return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(weight) || !aligned16(d_weight)) return LMHEAD_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (!accumulate_dweight &&
+        cudaMemsetAsync(d_weight, 0, sizeof(float) * static_cast<size_t>(V) * H, s) != cudaSuccess)
+      return LMHEAD_ERR_CUDA;
+    return LMHEAD_OK;
+  }
+  if (!hidden || !targets || !logp || !lse || !d_hidden || !workspace ||
+      (grad_entropy && !entropy))
+    return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(d_hidden) || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return LMHEAD_ERR_UNSUPPORTED;
+  if (workspace_bytes < lmhead_workspace_size(LMHEAD_OP_FWD_BWD, T, H, V, chunk_size))
+    return LMHEAD_ERR_WORKSPACE_TOO_SMALL;
+
+  const FusedPlan fp = plan_fused(T, H, V, chunk_size);
+  const bool keep = strategy == LMHEAD_STRATEGY_KEEP_LOGITS ||
+                    (strategy == LMHEAD_STRATEGY_AUTO && fp.preferred);
+  if (!keep) {
+    rc = lmhead_logps_fwd(hidden, weight, targets, loss_mask, T, H, V, temperature, chunk_size,
+                          logp, entropy, lse, workspace, workspace_bytes, stream);
+    if (rc != LMHEAD_OK) return rc;
+    return lmhead_logps_bwd(hidden, weight, targets, loss_mask, T, H, V, temperature, chunk_size,
+                            grad_logp, grad_entropy, lse, entropy, d_hidden, d_weight,
+                            accumulate_dweight, workspace, workspace_bytes, stream);
+  }
+
+  const int sms = sm_count();
+  if (sms <= 0) return LMHEAD_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  const Layout L = layout(LMHEAD_OP_FWD_BWD, T, H, V, chunk_size);
+  Front f;
+  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  if (rc != LMHEAD_OK) return rc;
+  if (loss_mask) {
+    LMH_TRY(launch("zero_masked_outputs", s, [&] {
+      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse, s);
+    }));
+    LMH_TRY(launch("zero_masked_rows", s, [&] {
+      return launch_zero_masked_rows(loss_mask, static_cast<int>(T), H, d_hidden, s);
+    }));
+  }
+  float4* part = reinterpret_cast<float4*>(ws + L.part);
+  float4* coef = reinterpret_cast<float4*>(ws + L.coef);
+  uint16_t* zbuf = reinterpret_cast<uint16_t*>(ws + L.dz);
+  float* m_tile = reinterpret_cast<float*>(ws + L.m_tile);
+  const bool pair = use_pair();
+  const int64_t um = unit_rows();
+  const int64_t ctas = pair ? 2 : 1;
+  const int splits = choose_splits(ceil_div(fp.Tb, um), fp.n_tiles, pair ? sms / 2 : sms);
+  const float scale = kLog2e / temperature;
+
+  for (int64_t tb = 0; tb < fp.n_tb; ++tb) {
+    const int64_t t0 = tb * fp.Tb;
+    if (t0 >= f.T_alloc) break;
+    const int64_t m_cap = std::min<int64_t>(fp.Tb, f.T_alloc - t0);
+    const int64_t h_rows = std::min<int64_t>(fp.Tb, f.rows_avail - t0);
+    const uint16_t* h_blk = f.h_src + t0 * H;
+    int* counter = f.counters + 2 * tb;
+
+    // forward over the whole vocabulary for this block, keeping the logits
+    LaunchArgs lf;
+    std::memset(&lf, 0, sizeof(lf));
+    if (!make_map(&lf.map_a[0], h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
+    if (!make_map(&lf.map_b[0], weight, H, V, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
+    if (!make_map_f16(&lf.map_out[0], zbuf, V, m_cap, 2ull * fp.V_pad, 64, BM))
+      return LMHEAD_ERR_CUDA;
+    GemmArgs& pf = lf.prob[0].p;
+    pf.m_cap = static_cast<int>(m_cap);
+    pf.n_extent = V;
+    pf.k_cap = H;
+    pf.m_dynamic = 1;
+    pf.dyn_base = static_cast<int>(t0);
+    pf.dev_rows = &f.st->rows;
+    pf.n_splits = splits;
+    pf.status = &f.st->status;
+    pf.scale = scale;
+    pf.row_base = static_cast<int>(t0);
+    pf.y_c = f.y_c;
+    pf.partials = part;
+    pf.part_ld = static_cast<int>(f.T_alloc);
+    pf.m_tile = m_tile;
+    pf.m_tile_ld = static_cast<int>(fp.n_tiles);
+    pf.out_mode = 1;
+    lf.n_problems = 1;
+    lf.counter = counter;
+    const int gf = static_cast<int>(
+        std::min<int64_t>(ceil_div(m_cap, um) * splits * ctas, sms));
+    LMH_TRY(launch("fwd_keep_gemm", s, [&] { return launch_gemm_fwd_z(lf, gf, pair, s); }));
+
+    const int r0 = static_cast<int>(t0), r1 = static_cast<int>(t0 + m_cap);
+    LMH_TRY(launch("fwd_merge", s, [&] {
+      return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st, r0,
+                              r1, logp, entropy, lse, s);
+    }));
+    LMH_TRY(launch("bwd_prep", s, [&] {
+      return launch_bwd_prep(f.idx, f.st, r0, r1, lse, entropy, grad_logp, grad_entropy,
+                             temperature, coef, s);
+    }));
+    LMH_TRY(launch("keep_dz", s, [&] {
+      return launch_fused_dz(zbuf, static_cast<int>(fp.V_pad), m_tile,
+                             static_cast<int>(fp.n_tiles), coef, f.y_c, f.st, r0,
+                             static_cast<int>(m_cap), V, s);
+    }));
+
+    // both gradient contractions over the whole vocabulary
+    LaunchArgs lg;
+    std::memset(&lg, 0, sizeof(lg));
+    if (!make_map(&lg.map_a[0], zbuf, V, m_cap, 2ull * fp.V_pad, BK, BM)) return LMHEAD_ERR_CUDA;
+    if (!make_map(&lg.map_b[0], weight, H, V, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+    GemmArgs& ph = lg.prob[0].p;
+    lg.prob[0].a_mn = 0;
+    ph.m_cap = static_cast<int>(m_cap);
+    ph.n_extent = H;
+    ph.k_cap = V;
+    ph.m_dynamic = 1;
+    ph.dyn_base = static_cast<int>(t0);
+    ph.dev_rows = &f.st->rows;
+    ph.status = &f.st->status;
+    ph.row_base = static_cast<int>(t0);
+    ph.out = d_hidden;
+    ph.out_ld = H;
+    ph.row_map = f.idx;
+    ph.accumulate = 0;
+    ph.n_fastest = 1;
+    if (!f.idx) {
+      ph.out_mode = 1;
+      if (!make_out_map_f32(&lg.map_out[0], d_hidden + t0 * H, H,
+                            std::min<int64_t>(m_cap, T - t0), H))
+        return LMHEAD_ERR_CUDA;
+    }
+    if (!make_map(&lg.map_a[1], zbuf, V, m_cap, 2ull * fp.V_pad, 64, 64)) return LMHEAD_ERR_CUDA;
+    if (!make_map(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+    GemmArgs& pw = lg.prob[1].p;
+    lg.prob[1].a_mn = 1;
+    pw.m_cap = V;
+    pw.n_extent = H;
+    pw.k_cap = static_cast<int>(m_cap);
+    pw.k_dynamic = 1;
+    pw.dyn_base = static_cast<int>(t0);
+    pw.dev_rows = &f.st->rows;
+    pw.status = &f.st->status;
+    pw.out = d_weight;
+    pw.out_ld = H;
+    pw.accumulate = (tb > 0 || accumulate_dweight) ? 1 : 0;
+    pw.zero_if_empty = 1;
+    pw.n_fastest = 1;
+    pw.out_mode = pw.accumulate ? 2 : 1;
+    if (!make_out_map_f32(&lg.map_out[1], d_weight, H, V, H)) return LMHEAD_ERR_CUDA;
+    lg.n_problems = 2;
+    lg.counter = counter + 1;
+    const int gg = static_cast<int>(std::min<int64_t>(
+        (ceil_div(m_cap, um) + ceil_div(V, um)) * ceil_div(H, BN) * ctas, sms));
+    LMH_TRY(launch("bwd_grad_gemm", s, [&] { return launch_gemm_bwd_grad(lg, gg, pair, s); }));
+  }
+  return LMHEAD_OK;
+}
+
 lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream) {
   if (!workspace) return LMHEAD_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -595,5 +819,13 @@ lmhead_status lmhead_profile_record(int i, const char** name, float* ms) {
 }
 
 uint64_t lmhead_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int lmhead_fwd_bwd_keeps_logits(int64_t T, int32_t H, int32_t V, int32_t chunk_size,
+                                int32_t* block_tokens) {
+  if (check_sizes(T, H, V, 1.0f, chunk_size) != LMHEAD_OK || T == 0) return -1;
+  const FusedPlan fp = plan_fused(T, H, V, chunk_size);
+  if (block_tokens) *block_tokens = static_cast<int32_t>(fp.Tb);
+  return fp.preferred ? 1 : 0;
+}
 
 }  // extern "C"

@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int y = -1;
       bool row_ok = false;
       int64_t orow = 0;
-      if constexpr (EPI == EPI_FWD_STATS) {
+      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_Z) {
         row_ok = row < s.M;
         if (row_ok) y = p.y_c[p.row_base + row];
       } else if constexpr (EPI == EPI_BWD_DZ) {
@@ -593,6 +593,76 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 if (j == yt - cb) zy = v[j] * p.scale;
             }
           }
+        } else if constexpr (EPI == EPI_FWD_Z) {
+          // pass 1: the tile's maximum sets this tile's reference m' (>= every
+          // logit in it), so the kept values u - m' are <= 0 and fp16 keeps
+          // most precision where p is largest
+          float tmax = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load_32(tcol + c * 32, v);
+            const int lim = p.n_extent - col0 - c * 32;
+            if (lim >= 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < lim) tmax = fmaxf(tmax, v[j]);
+            }
+          }
+          const float cm = tmax * p.scale;
+          if (cm > mrun) {
+            const float dm = mrun - cm;
+            const float r = ex2_approx(dm);
+            s1 = ssum > 0.f ? r * fmaf(dm, ssum, s1) : 0.f;
+            ssum *= r;
+            mrun = cm;
+          }
+          const float mref = mrun;
+          // pass 2: statistics from the same exponentials, and the kept logits
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 64; ++cc) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float v[32];
+              tmem_load_32(tcol + cc * 64 + h * 32, v);
+              if (cc == BN / 64 - 1 && h == 1) release_acc();
+              const int cb = cc * 64 + h * 32;
+              const int lim = p.n_extent - col0 - cb;
+              float d[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) d[j] = fmaf(v[j], p.scale, -mref);
+              if (lim >= 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const float e = ex2_approx(d[j]);
+                  ssum += e;
+                  s1 = fmaf(e, d[j], s1);
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  if (j < lim) {
+                    const float e = ex2_approx(d[j]);
+                    ssum += e;
+                    s1 = fmaf(e, d[j], s1);
+                  }
+                }
+              }
+              if (static_cast<unsigned>(yt - cb) < 32u) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j == yt - cb) zy = v[j] * p.scale;
+              }
+#pragma unroll
+              for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_f16x2(d[2 * k], d[2 * k + 1]);
+            }
+            stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t);
+          }
+          if (row < p.m_cap) p.m_tile[static_cast<int64_t>(row) * p.m_tile_ld + n] = mref;
         } else if constexpr (EPI == EPI_BWD_DZ) {
           // 64 columns per staged chunk: 128 bytes of bf16 per row
 #pragma unroll 1
@@ -679,9 +749,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (acc == 0) acc_phase ^= 1;
       }
       if (!ok) break;
-      if constexpr (EPI == EPI_FWD_STATS) {
+      if constexpr (EPI == EPI_FWD_STATS || EPI == EPI_FWD_Z) {
         if (row_ok)
-          p.partials[static_cast<int64_t>(split) * p.part_ld + row] =
+          p.partials[static_cast<int64_t>(split) * p.part_ld + p.row_base + row] =
               make_float4(mrun, ssum, s1, zy);
       }
     }

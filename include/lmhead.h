@@ -76,12 +76,19 @@ typedef enum {
   LMHEAD_ERR_BAD_TARGET = 6      /* a scored target outside [-V, V) */
 } lmhead_status;
 
-enum { LMHEAD_OP_FWD = 0, LMHEAD_OP_BWD = 1 };
+enum { LMHEAD_OP_FWD = 0, LMHEAD_OP_BWD = 1, LMHEAD_OP_FWD_BWD = 2 };
+
+/* How lmhead_logps_fwd_bwd runs (see there). */
+enum {
+  LMHEAD_STRATEGY_AUTO = 0,        /* the library's cost model chooses */
+  LMHEAD_STRATEGY_RECOMPUTE = 1,   /* lmhead_logps_fwd, then lmhead_logps_bwd */
+  LMHEAD_STRATEGY_KEEP_LOGITS = 2  /* keep each token block's logits; no recompute */
+};
 
 /*
- * Bytes of device workspace that lmhead_logps_fwd (op = LMHEAD_OP_FWD) or
- * lmhead_logps_bwd (op = LMHEAD_OP_BWD) needs for these sizes; 0 for invalid
- * sizes.  The workspace holds the compacted scored rows (2*T*H bytes at
+ * Bytes of device workspace that lmhead_logps_fwd (op = LMHEAD_OP_FWD),
+ * lmhead_logps_bwd (op = LMHEAD_OP_BWD) or lmhead_logps_fwd_bwd (op =
+ * LMHEAD_OP_FWD_BWD, any strategy) needs for these sizes; 0 for invalid sizes.  The workspace holds the compacted scored rows (2*T*H bytes at
  * most), per-token statistics (tens of bytes per token) and, for the
  * backward, a bf16 logit-cotangent block of at most about chunk_size * V
  * elements.  It never grows with T * V: chunk_size alone bounds the
@@ -142,6 +149,50 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
                                const float* lse, const float* entropy, float* d_hidden,
                                float* d_weight, int accumulate_dweight, void* workspace,
                                size_t workspace_bytes, lmhead_stream_t stream);
+
+/*
+ * Forward and backward in one call, for losses whose per-token cotangents
+ * are known before the forward (a GRPO-style sum of advantage-weighted
+ * log-probs plus an entropy term; tunix PR #2913, commit "fused sharded
+ * log-prob head": one cotangent, read by both gradient matmuls).
+ *
+ * Arguments and results are those of lmhead_logps_fwd followed by
+ * lmhead_logps_bwd with the same cotangents (entropy is required when
+ * grad_entropy is given).  `strategy`:
+ *  LMHEAD_STRATEGY_RECOMPUTE    exactly the two calls (logits recomputed in
+ *                               the backward);
+ *  LMHEAD_STRATEGY_KEEP_LOGITS  token blocks of T_b tokens spanning the whole
+ *                               vocabulary (T_b x V <= chunk_size x V): the
+ *                               forward keeps the block's logits (16-bit, relative
+ *                               to each 256-column tile's running maximum), one
+ *                               elementwise pass turns them into the cotangent,
+ *                               and no logit is recomputed.  Counted flops stay
+ *                               6 T H V, executed flops drop from 8 to 6 T H V;
+ *                               results agree with RECOMPUTE within the
+ *                               head's tolerances, not bit for bit;
+ *  LMHEAD_STRATEGY_AUTO         whichever the library's cost model expects to
+ *                               be faster (KEEP_LOGITS needs large chunks, since
+ *                               its smaller token blocks add fp32 passes over
+ *                               d_weight; lmhead_fwd_bwd_keeps_logits reports the
+ *                               choice).
+ * workspace: at least lmhead_workspace_size(LMHEAD_OP_FWD_BWD, ...) bytes.
+ */
+lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weight,
+                                   const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                                   int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                                   const float* grad_logp, const float* grad_entropy,
+                                   float* logp, float* entropy, float* lse, float* d_hidden,
+                                   float* d_weight, int accumulate_dweight, int strategy,
+                                   void* workspace, size_t workspace_bytes,
+                                   lmhead_stream_t stream);
+
+/*
+ * 1 if LMHEAD_STRATEGY_AUTO keeps the logits for these sizes, 0 if it
+ * recomputes them, -1 for invalid sizes; *block_tokens (if not NULL) gets the
+ * token block T_b that KEEP_LOGITS would use.
+ */
+int lmhead_fwd_bwd_keeps_logits(int64_t T, int32_t H, int32_t V, int32_t chunk_size,
+                                int32_t* block_tokens);
 
 /*
  * Synchronises `stream`, then returns the device status word that the last

@@ -111,3 +111,36 @@ def assert_parity(gpu, ora, rows=None, keys=("logp", "entropy", "lse", "d_hidden
     bad = {k: v for k, v in e.items() if not v <= LIMITS[k]}
     assert not bad, "parity failed: %s (all: %s)" % (bad, e)
     return e
+
+
+def run_gpu_fwd_bwd(x, strategy, chunk=None, tau=None, grad_entropy=True, grad_logp=True,
+                    accumulate=False, d_weight_init=None, with_entropy=True):
+    """lmhead_logps_fwd_bwd on cuda:0; numpy results and the device status."""
+    ensure_built()
+    g = to_device(x)
+    T, H = g["hidden"].shape
+    V = g["weight"].shape[0]
+    chunk = chunk or x["chunk_size"]
+    tau = x["temperature"] if tau is None else tau
+    ws = torch.empty(lm.lmhead_workspace_size(2, T, H, V, chunk), dtype=torch.uint8,
+                     device="cuda")
+    logp = torch.empty(T, device="cuda")
+    ent = torch.empty(T, device="cuda") if with_entropy else None
+    lse = torch.empty(T, device="cuda")
+    dh = torch.empty((T, H), device="cuda")
+    dw = (torch.empty((V, H), device="cuda") if d_weight_init is None
+          else d_weight_init.to("cuda").clone())
+    rc = lm.lmhead_logps_fwd_bwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau,
+                                 chunk, g["grad_logp"] if grad_logp else None,
+                                 g["grad_entropy"] if grad_entropy else None, logp, ent, lse, dh,
+                                 dw, accumulate, strategy, ws)
+    assert rc == 0, lm.STATUS_NAMES.get(rc)
+    out = {"status": lm.lmhead_read_device_status(ws)}
+    torch.cuda.synchronize()
+    out["logp"] = logp.cpu().double().numpy()
+    if with_entropy:
+        out["entropy"] = ent.cpu().double().numpy()
+    out["lse"] = lse.cpu().double().numpy()
+    out["d_hidden"] = dh.cpu().double().numpy()
+    out["d_weight"] = dw.cpu().double().numpy()
+    return out

@@ -48,7 +48,8 @@ def test_workspace_size_invalid(lib):
     assert lm.lmhead_workspace_size(0, 10, 64, 0, 8) == 0
     assert lm.lmhead_workspace_size(0, 10, 64, 10, 0) == 0
     assert lm.lmhead_workspace_size(0, 10, 65, 10, 8) == 0     # H % 64 != 0
-    assert lm.lmhead_workspace_size(2, 10, 64, 10, 8) == 0     # unknown op
+    assert lm.lmhead_workspace_size(3, 10, 64, 10, 8) == 0     # unknown op
+    assert lm.lmhead_workspace_size(-1, 10, 64, 10, 8) == 0
 
 
 @pytest.mark.parametrize("T,H,V,c", [(4096, 2560, 151936, 512), (65536, 2560, 151936, 512),
@@ -125,6 +126,43 @@ def test_backward_argument_errors(lib):
     assert call(dw=_fake((1 << 20) + 4)) == 2
     assert call(wsb=100) == 3
     assert call(T=0, acc=1, h=None, y=None, ls=None, dh=None, wsp=None) == 0
+
+
+@pytest.mark.parametrize("T,H,V,c", [(4096, 2560, 151936, 512), (65536, 4096, 151936, 4096),
+                                     (200000, 2048, 151936, 4096), (300, 192, 3001, 64)])
+def test_fwd_bwd_workspace_and_plan(lib, T, H, V, c):
+    """The single-call workspace covers every strategy and stays chunk-bounded."""
+    ws = lm.lmhead_workspace_size(2, T, H, V, c)
+    assert ws >= lm.lmhead_workspace_size(0, T, H, V, c)
+    assert ws >= lm.lmhead_workspace_size(1, T, H, V, c)
+    keep, tb = lm.lmhead_fwd_bwd_keeps_logits(T, H, V, c)
+    Vp = (V + 255) // 256 * 256
+    assert tb % 256 == 0 and (tb * Vp <= c * V or tb == 256)
+    Ta = (T + 127) // 128 * 128
+    # logits block (2 B) + per-tile maxima (4 B per 256 columns): no T x V term
+    assert ws <= Ta * (8 + 2 * H + 16 * 32 + 16) + 2 * tb * Vp + 4 * tb * (Vp // 256) + \
+        2 * (c * V + 128 * 256 + 256 * Ta + 128 * V) + 16 * 256
+
+
+def test_fwd_bwd_argument_errors(lib):
+    f = lib.lmhead_logps_fwd_bwd
+    A = _fake(1 << 20)
+    ws = _fake(1 << 24)
+
+    def call(h=A, w=A, y=A, m=None, T=8, H=64, V=10, tau=1.0, c=4, gl=A, ge=None, lp=A, en=None,
+             ls=A, dh=A, dw=A, acc=0, strat=0, wsp=ws, wsb=1 << 40):
+        return f(h, w, y, m, T, H, V, tau, c, gl, ge, lp, en, ls, dh, dw, acc, strat, wsp, wsb,
+                 None)
+
+    assert call(strat=3) == 1
+    assert call(strat=-1) == 1
+    assert call(tau=0.0) == 1
+    assert call(H=96) == 2
+    assert call(ge=A, en=None) == 1
+    assert call(lp=None) == 1
+    assert call(dh=_fake((1 << 20) + 4)) == 2
+    assert call(wsb=64) == 3
+    assert call(T=0, acc=1, h=None, y=None, lp=None, ls=None, dh=None, wsp=None) == 0
 
 
 def test_plan_is_chunk_bounded(lib):

@@ -79,3 +79,29 @@ def test_sparse_cotangent_full_dweight(case):
     others[rows] = False
     assert np.all(g["d_hidden"][others] == 0.0)
     print(w.name, e)
+
+
+@pytest.mark.parametrize("name", ["packed_long_row", "long_trace"])
+def test_single_call_keep_logits_full_size(name):
+    """The single-call path at full size, with the strategy the cost model picks
+    (it keeps the logits at chunk 4096): sampled rows and, with cotangents on a
+    token sample, the whole d_weight against the oracle."""
+    import chunked_lm_head_tcgen05_gb300 as lm
+    from gpu_helpers import run_gpu_fwd_bwd
+    w = W.WORKLOADS[name]
+    keep, _ = lm.lmhead_fwd_bwd_keeps_logits(w.T, w.H, w.V, w.chunk_size)
+    assert keep
+    x = W.make_inputs(w)
+    rows, _ = _sample_rows(x, 6, 0, 3)
+    keepmask = torch.zeros(w.T)
+    keepmask[torch.from_numpy(rows)] = 1.0
+    x["grad_logp"] = x["grad_logp"] * keepmask
+    x["grad_entropy"] = x["grad_entropy"] * keepmask
+    g = run_gpu_fwd_bwd(x, 0)
+    assert g["status"] == 0
+    o = run_oracle(x, rows=rows)
+    e = assert_parity(g, o, rows=rows, keys=("logp", "entropy", "lse"))
+    e["d_weight"] = rel_fro(g["d_weight"], o["d_weight"])
+    e["d_hidden"] = rel_fro(g["d_hidden"][rows], o["d_hidden"])
+    assert e["d_weight"] <= LIMITS["d_weight"] and e["d_hidden"] <= LIMITS["d_hidden"], e
+    print(name, e)
