@@ -328,3 +328,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 }  // namespace lmh
+
+namespace lmh {
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue early, and wait for the previous kernel's results before use.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+}  // namespace lmh

@@ -196,15 +196,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t rank = PAIR ? cluster_cta_rank() : 0u;
   const bool leader = rank == 0;
 
-  Sched sc0, sc1;
-  sc0.init(L.prob[0].p, C::UNIT_M);
-  if (L.n_problems > 1) {
-    sc1.init(L.prob[1].p, C::UNIT_M);
-  } else {
-    sc1 = sc0;
-    sc1.units = 0;
-  }
-  const int total_units = sc0.units + sc1.units;
+  // The next kernel in the stream may begin its own prologue once every CTA
+  // of this one is resident; it waits for this grid's results before use.
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -239,6 +233,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort = &ctl->abort;
   const uint32_t smem_base = smem_addr(smem);
+
+  // Everything above only touched this CTA's own resources; inputs written
+  // by earlier kernels (scored count, counters, operands) are read below.
+  pdl_wait_prerequisites();
+  Sched sc0, sc1;
+  sc0.init(L.prob[0].p, C::UNIT_M);
+  if (L.n_problems > 1) {
+    sc1.init(L.prob[1].p, C::UNIT_M);
+  } else {
+    sc1 = sc0;
+    sc1.units = 0;
+  }
+  const int total_units = sc0.units + sc1.units;
 
   // scheduler ring: the even CTA fetches, the odd CTA reads its copy
   auto sched_take = [&](int slot, uint32_t spar, int& u) -> bool {
@@ -802,29 +809,34 @@ cudaError_t launch_tc_gemm(const LaunchArgs& a, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(GEMM_SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  if constexpr (!PAIR) {
-    kern<<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(a);
-    return cudaGetLastError();
-  } else {
+  int ctas = grid < 1 ? 1 : grid;
+  if constexpr (PAIR) {
     const int pairs_max = max_active_pairs(kern);
     if (pairs_max <= 0) return cudaErrorInvalidConfiguration;
-    int pairs = (grid + 1) / 2;
+    int pairs = (ctas + 1) / 2;
     if (pairs > pairs_max) pairs = pairs_max;
-    if (pairs < 1) pairs = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    ctas = 2 * pairs;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if constexpr (PAIR) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace lmh
