@@ -61,6 +61,12 @@ class Oracle:
         lib.lmo_backward.argtypes = [_I64, _I32, _I32, _VP, ctypes.c_int, _VP, ctypes.c_int,
                                      _VP, _VP, ctypes.c_double, _VP, _VP, _VP, _VP]
         lib.lmo_num_threads.restype = ctypes.c_int
+        lib.lmo_logits_forward.restype = ctypes.c_int
+        lib.lmo_logits_forward.argtypes = [_I64, _I32, _VP, _VP, _VP, ctypes.c_double, _VP, _VP,
+                                           _VP]
+        lib.lmo_logits_backward.restype = ctypes.c_int
+        lib.lmo_logits_backward.argtypes = [_I64, _I32, _VP, _VP, _VP, ctypes.c_double, _VP, _VP,
+                                            _VP]
         self._lib = lib
 
     def num_threads(self):
@@ -101,6 +107,35 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle backward failed with code %d" % rc)
         return dh, dw
+
+
+    def logits_forward(self, logits, targets, mask, temperature):
+        """Scoring of given logits [T,V] (float64): (logp, entropy, lse)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float64)
+        T, V = logits.shape
+        y = _vec(targets, T, np.int32, "targets")
+        m = _vec(mask, T, np.uint8, "mask")
+        out = [np.empty(T, np.float64) for _ in range(3)]
+        rc = self._lib.lmo_logits_forward(T, V, _ptr(logits), _ptr(y), _ptr(m), float(temperature),
+                                          *[_ptr(a) for a in out])
+        if rc != 0:
+            raise ValueError("oracle logits forward failed with code %d" % rc)
+        return tuple(out)
+
+    def logits_backward(self, logits, targets, mask, temperature, grad_logp, grad_entropy):
+        """d loss / d logits [T,V] (float64)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float64)
+        T, V = logits.shape
+        y = _vec(targets, T, np.int32, "targets")
+        m = _vec(mask, T, np.uint8, "mask")
+        gl = _vec(grad_logp, T, np.float64, "grad_logp")
+        ge = _vec(grad_entropy, T, np.float64, "grad_entropy")
+        d = np.empty((T, V), np.float64)
+        rc = self._lib.lmo_logits_backward(T, V, _ptr(logits), _ptr(y), _ptr(m), float(temperature),
+                                           _ptr(gl), _ptr(ge), _ptr(d))
+        if rc != 0:
+            raise ValueError("oracle logits backward failed with code %d" % rc)
+        return d
 
 
 _default = None

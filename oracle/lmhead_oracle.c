@@ -248,3 +248,124 @@ int lmo_backward(int64_t T, int32_t H, int32_t V,
   free(ent_t);
   return failed ? -2 : 0;
 }
+
+/*
+ * Logits-level scoring (for callers that already hold a chunk's logits).
+ * The pages test their fused scoring on logits with inf, -inf and NaN
+ * entries and a row of no finite logit, and list the isfinite mask of the
+ * cotangent among the parts a test must catch (tunix PR #2913, commit
+ * "fused sharded log-prob head": FusedScoringTest), but print no values.
+ * This file reads them as follows, with z = logits / tau per row:
+ *   - an entry of -inf has probability 0 and contributes nothing (the limit
+ *     of the definition); its cotangent is 0 (isfinite mask);
+ *   - a NaN or +inf entry anywhere in the row makes lse, logp and entropy
+ *     NaN; finite entries' cotangents are then NaN, non-finite ones 0;
+ *   - a row with no finite entry has lse = -inf, logp = NaN, entropy = NaN
+ *     and an all-zero cotangent;
+ *   - otherwise lse, logp, entropy and the cotangent are those of the head
+ *     over the finite entries (logp = -inf when the target's logit is -inf).
+ * Unscored rows give zeros; invalid targets give logp = NaN (as above).
+ */
+static int row_has_nan_or_posinf(const double* z, int32_t V) {
+  for (int32_t v = 0; v < V; ++v)
+    if (isnan(z[v]) || (isinf(z[v]) && z[v] > 0)) return 1;
+  return 0;
+}
+
+static void logits_row_statistics(const double* z, int32_t V, double* lse_out, double* ent_out) {
+  if (row_has_nan_or_posinf(z, V)) {
+    *lse_out = NAN;
+    *ent_out = NAN;
+    return;
+  }
+  double m = -INFINITY;
+  for (int32_t v = 0; v < V; ++v) m = z[v] > m ? z[v] : m;
+  if (!isfinite(m)) {  /* no finite entry */
+    *lse_out = -INFINITY;
+    *ent_out = NAN;
+    return;
+  }
+  double s = 0.0;
+  for (int32_t v = 0; v < V; ++v)
+    if (isfinite(z[v])) s += exp(z[v] - m);
+  double lse = m + log(s);
+  double spz = 0.0;
+  for (int32_t v = 0; v < V; ++v)
+    if (isfinite(z[v])) spz += exp(z[v] - lse) * z[v];
+  *lse_out = lse;
+  *ent_out = lse - spz;
+}
+
+int lmo_logits_forward(int64_t T, int32_t V, const double* logits, const int32_t* targets,
+                       const uint8_t* mask, double tau, double* logp, double* entropy,
+                       double* lse) {
+  if (T < 0 || V <= 0 || !(tau > 0.0) || !isfinite(tau)) return -1;
+  if (T == 0) return 0;
+  if (!logits || !targets || !logp || !entropy || !lse) return -1;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!z) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+      if (!z) continue;
+      if (mask && !mask[t]) {
+        logp[t] = entropy[t] = lse[t] = 0.0;
+        continue;
+      }
+      const double* row = logits + t * (int64_t)V;
+      for (int32_t v = 0; v < V; ++v) z[v] = row[v] / tau;
+      double L, E;
+      logits_row_statistics(z, V, &L, &E);
+      int64_t y = wrapped_target(targets[t], V);
+      logp[t] = (y >= 0) ? z[y] - L : NAN;
+      entropy[t] = E;
+      lse[t] = L;
+    }
+    free(z);
+  }
+  return failed ? -2 : 0;
+}
+
+/* d_logits [T,V] overwritten: d loss / d logits (the 1/tau of z = logits/tau included). */
+int lmo_logits_backward(int64_t T, int32_t V, const double* logits, const int32_t* targets,
+                        const uint8_t* mask, double tau, const double* grad_logp,
+                        const double* grad_entropy, double* d_logits) {
+  if (T < 0 || V <= 0 || !(tau > 0.0) || !isfinite(tau)) return -1;
+  if (T == 0) return 0;
+  if (!logits || !targets || !d_logits) return -1;
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!z) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t t = 0; t < T; ++t) {
+      double* dz = d_logits + t * (int64_t)V;
+      for (int32_t v = 0; v < V; ++v) dz[v] = 0.0;
+      if (!z || (mask && !mask[t])) continue;
+      const double* row = logits + t * (int64_t)V;
+      for (int32_t v = 0; v < V; ++v) z[v] = row[v] / tau;
+      double L, E;
+      logits_row_statistics(z, V, &L, &E);
+      double gl = grad_logp ? grad_logp[t] : 0.0;
+      double ge = grad_entropy ? grad_entropy[t] : 0.0;
+      int64_t y = wrapped_target(targets[t], V);
+      for (int32_t v = 0; v < V; ++v) {
+        if (!isfinite(z[v])) continue;          /* isfinite mask */
+        double p = exp(z[v] - L);
+        double onehot = (v == y) ? 1.0 : 0.0;
+        dz[v] = (gl * (onehot - p) - ge * p * (z[v] - L + E)) / tau;
+      }
+    }
+    free(z);
+  }
+  return failed ? -2 : 0;
+}

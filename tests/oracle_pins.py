@@ -306,6 +306,85 @@ def pin_bf16_storage(o):
         assert np.array_equal(u, v)
 
 
+def _logits_via_head(o, logits, y, mask, tau, gl, ge):
+    """Score logits with the hidden-state oracle: hidden = one-hot rows,
+    W[v, t] = logits[t, v], so z[t, v] = logits[t, v] / tau; d logits[t, v]
+    is then d_weight[v, t]."""
+    T, V = logits.shape
+    h = np.eye(T)
+    W = np.ascontiguousarray(logits.T)
+    f = o.forward(h, W, y, mask, tau)
+    _, dw = o.backward(h, W, y, mask, tau, gl, ge)
+    return f, np.ascontiguousarray(dw.T)
+
+
+def pin_logits_match_head(o):
+    """Finite logits: the logits-level scoring equals the head's definition."""
+    r = _rng(12)
+    T, V, tau = 7, 40, 0.7
+    logits = r.normal(size=(T, V)) * 2
+    y = r.integers(-V, V, size=T).astype(np.int32)
+    mask = np.array([1, 1, 0, 1, 1, 1, 1], np.uint8)
+    gl, ge = r.normal(size=T), r.normal(size=T)
+    (hl, he, hs), hd = _logits_via_head(o, logits, y, mask, tau, gl, ge)
+    lp, en, ls = o.logits_forward(logits, y, mask, tau)
+    d = o.logits_backward(logits, y, mask, tau, gl, ge)
+    _close(lp, hl, 1e-12, 1e-12, "logits logp")
+    _close(en, he, 1e-12, 1e-12, "logits entropy")
+    _close(ls, hs, 1e-12, 1e-12, "logits lse")
+    _close(d, hd, 1e-12, 1e-10, "logits gradient")
+
+
+def pin_logits_neg_inf_is_removal(o):
+    """-inf entries behave as if those vocabulary entries were absent, and get
+    a zero cotangent (isfinite mask); a -inf target logit gives logp = -inf."""
+    r = _rng(13)
+    V, tau = 30, 0.9
+    row = r.normal(size=V)
+    gone = np.array([1, 5, 6, 17, 29])
+    row[gone] = -np.inf
+    keep = np.setdiff1d(np.arange(V), gone)
+    y = np.array([8, 5], np.int32)            # a kept id, then a -inf id
+    gl, ge = np.array([0.7, 1.3]), np.array([-0.4, 0.8])
+    z = np.stack([row, row])
+    lp, en, ls = o.logits_forward(z, y, None, tau)
+    d = o.logits_backward(z, y, None, tau, gl, ge)
+    short = row[keep][None, :]
+    ys = np.array([int(np.searchsorted(keep, 8))], np.int32)
+    (hl, he, hs), hd = _logits_via_head(o, short, ys, None, tau, gl[:1], ge[:1])
+    _close(lp[0], hl[0], 1e-12, 1e-12, "removal logp")
+    _close(en, he[0], 1e-12, 1e-12, "removal entropy")
+    _close(ls, hs[0], 1e-12, 1e-12, "removal lse")
+    assert lp[1] == -np.inf
+    assert np.all(d[:, gone] == 0.0)
+    _close(d[0, keep], hd[0], 1e-12, 1e-10, "removal gradient")
+    # the -inf target: no one-hot term, the rest as for a target of zero weight
+    (h2, _, _), hd2 = _logits_via_head(o, short, np.array([-1000], np.int32), None, tau,
+                                       np.array([gl[1]]), np.array([ge[1]]))
+    assert np.isnan(h2[0])
+    _close(d[1, keep], hd2[0], 1e-12, 1e-10, "-inf target gradient")
+
+
+def pin_logits_nonfinite_rows(o):
+    """NaN or +inf anywhere -> NaN statistics, NaN cotangent on finite entries,
+    zero on the rest; a row with no finite logit -> lse = -inf, logp and
+    entropy NaN, zero cotangent."""
+    V = 6
+    z = np.array([[0.1, np.nan, 0.3, -np.inf, 1.0, 2.0],
+                  [0.1, np.inf, 0.3, -np.inf, 1.0, 2.0],
+                  [-np.inf] * V,
+                  [0.5, -1.0, 0.0, 2.0, -np.inf, 1.0]])
+    y = np.array([0, 0, 2, 3], np.int32)
+    lp, en, ls = o.logits_forward(z, y, None, 1.0)
+    d = o.logits_backward(z, y, None, 1.0, np.ones(4), np.ones(4))
+    for t in (0, 1):
+        assert np.isnan(lp[t]) and np.isnan(en[t]) and np.isnan(ls[t])
+        fin = np.isfinite(z[t])
+        assert np.all(np.isnan(d[t][fin])) and np.all(d[t][~fin] == 0.0)
+    assert ls[2] == -np.inf and np.isnan(lp[2]) and np.isnan(en[2]) and np.all(d[2] == 0.0)
+    assert np.all(np.isfinite([lp[3], en[3], ls[3]])) and d[3, 4] == 0.0
+
+
 ALL_PINS = [
     pin_zero_weight_forward,
     pin_one_hot_dominant,
@@ -320,4 +399,7 @@ ALL_PINS = [
     pin_dweight_column_sums,
     pin_masks_and_targets,
     pin_bf16_storage,
+    pin_logits_match_head,
+    pin_logits_neg_inf_is_removal,
+    pin_logits_nonfinite_rows,
 ]

@@ -42,6 +42,14 @@ MUTANTS = [
     ("dweight_transposed_h", "dw[k] += c * h[k];", "dw[k] += c * hrows[k * T + t];"),
     ("mask_ignored_fwd", "if (mask && !mask[t]) {\n        logp[t] = 0.0;", "if (0) {\n        logp[t] = 0.0;"),
     ("bf16_decode_shift", "(uint32_t)bits << 16;", "(uint32_t)bits << 15;"),
+    ("logits_isfinite_mask_dropped", "        if (!isfinite(z[v])) continue;          /* isfinite mask */\n", ""),
+    ("logits_posinf_treated_as_finite", "if (isnan(z[v]) || (isinf(z[v]) && z[v] > 0)) return 1;",
+     "if (isnan(z[v])) return 1;"),
+    ("logits_neg_inf_counted_in_sum", "    if (isfinite(z[v])) s += exp(z[v] - m);",
+     "    s += isfinite(z[v]) ? exp(z[v] - m) : exp(-1.0);"),
+    ("logits_tau_dropped_in_grad", "        dz[v] = (gl * (onehot - p) - ge * p * (z[v] - L + E)) / tau;",
+     "        dz[v] = (gl * (onehot - p) - ge * p * (z[v] - L + E));"),
+    ("logits_empty_row_entropy_zero", "    *lse_out = -INFINITY;\n    *ent_out = NAN;", "    *lse_out = -INFINITY;\n    *ent_out = 0.0;"),
 ]
 
 
