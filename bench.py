@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--workload", default="qwen3_4b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--op", choices=["head", "score_logits"], default="head",
+                    help="head: the hidden-state head (default); score_logits: the logits-level entry")
     ap.add_argument("--only-device", action="store_true",
                     help="time the device-resident steps only (profiling runs)")
     return ap.parse_args()
@@ -396,11 +398,83 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_score_logits(args, rank, world, local):
+    """Logits-level scoring of one chunk of logits (fp32 [512, 151936], the chunk of the
+    Qwen3-4B-shaped head): forward + backward, HBM-bound.  One JSON line."""
+    import torch
+    import chunked_lm_head_tcgen05_gb300 as lm
+    lm.build()
+    lm.library()
+    dev = torch.device("cuda", local)
+    T, V, tau = 512, 151936, 1.0
+    g = torch.Generator().manual_seed(20261202)
+    z = torch.randn((T, V), generator=g) * 2.0
+    z[torch.rand((T, V), generator=g) < 0.01] = float("-inf")
+    z = z.to(dev)
+    y = torch.randint(0, V, (T,), generator=g, dtype=torch.int64).to(torch.int32).to(dev)
+    gl = torch.randn(T, generator=g).to(dev)
+    ge = torch.randn(T, generator=g).to(dev)
+    logp, ent, lse = (torch.empty(T, device=dev) for _ in range(3))
+    dz = torch.empty_like(z)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rc = lm.lmhead_score_logits_fwd(z, y, None, tau, logp, ent, lse, stream)
+        rc |= lm.lmhead_score_logits_bwd(z, y, None, tau, gl, ge, lse, ent, dz, stream)
+        if rc:
+            raise lm.LmheadError(rc, "score_logits")
+
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = lm.lmhead_launch_count()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    lm.lmhead_profile_enable(1)
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    lm.lmhead_profile_enable(0)
+    per = {}
+    for i in range(lm.lmhead_profile_count()):
+        name, ms = lm.lmhead_profile_record(i)
+        per.setdefault(name, []).append(ms)
+    peaks, src = measured_peaks()
+    bytes_step = 12.0 * T * V
+    bwd_ms = sum(per["score_logits_bwd"]) / len(per["score_logits_bwd"])
+    achieved = 8.0 * T * V / (bwd_ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "tokens/s of logits-level log-prob + entropy scoring, fwd+bwd",
+            "value": T * world * args.steps / t, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "logits chunk [512, 151936] fp32, 1% -inf entries, tau=1",
+                       "l2": "inputs larger than L2 (311 MB of logits)"},
+            "gb_per_s": bytes_step * args.steps / t / 1e9,
+            "gpu_launches": lm.lmhead_launch_count() - n0 - 2 * 3,
+            "roofline": {"bound": "hbm", "kernel": "score_logits_bwd", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (of %s)" % src},
+            "kernels_ms": {k: sum(v) / len(v) for k, v in per.items()},
+        }), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.op == "score_logits":
+        run_score_logits(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

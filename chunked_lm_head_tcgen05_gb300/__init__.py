@@ -22,7 +22,8 @@ __all__ = [
     "lmhead_profile_record", "lmhead_launch_count", "lmhead_logps_fwd_noalloc",
     "NOALLOC_SCRATCH_BYTES", "lmhead_logps_fwd_bwd", "lmhead_fwd_bwd_keeps_logits",
     "LMHEAD_OP_FWD_BWD", "LMHEAD_STRATEGY_AUTO", "LMHEAD_STRATEGY_RECOMPUTE",
-    "LMHEAD_STRATEGY_KEEP_LOGITS", "forward", "backward",
+    "LMHEAD_STRATEGY_KEEP_LOGITS", "lmhead_score_logits_fwd", "lmhead_score_logits_bwd",
+    "forward", "backward",
 ]
 
 LMHEAD_OP_FWD = 0
@@ -72,6 +73,10 @@ _SIGNATURES = {
                                             _VP, ctypes.c_int, ctypes.c_int, _VP, _SZ, _VP]),
     "lmhead_fwd_bwd_keeps_logits": (ctypes.c_int, [_I64, _I32, _I32, _I32,
                                                    ctypes.POINTER(_I32)]),
+    "lmhead_score_logits_fwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.c_float, _VP,
+                                               _VP, _VP, _VP]),
+    "lmhead_score_logits_bwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.c_float, _VP,
+                                               _VP, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -234,6 +239,40 @@ def lmhead_fwd_bwd_keeps_logits(T, H, V, chunk_size):
     if r < 0:
         raise LmheadError(1, "lmhead_fwd_bwd_keeps_logits")
     return bool(r), tb.value
+
+
+def lmhead_score_logits_fwd(logits, targets, loss_mask, temperature, logp, entropy, lse,
+                            stream=None):
+    """C ``lmhead_score_logits_fwd`` on torch tensors; returns the status code."""
+    import torch
+    T, V = logits.shape
+    _check_tensor(logits, "logits", torch.float32, (T, V))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(logp, "logp", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    return int(library().lmhead_score_logits_fwd(
+        _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(logp),
+        _ptr(entropy), _ptr(lse), _stream(stream)))
+
+
+def lmhead_score_logits_bwd(logits, targets, loss_mask, temperature, grad_logp, grad_entropy,
+                            lse, entropy, d_logits, stream=None):
+    """C ``lmhead_score_logits_bwd`` on torch tensors; returns the status code."""
+    import torch
+    T, V = logits.shape
+    _check_tensor(logits, "logits", torch.float32, (T, V))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(grad_logp, "grad_logp", torch.float32, (T,), allow_none=True)
+    _check_tensor(grad_entropy, "grad_entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(d_logits, "d_logits", torch.float32, (T, V))
+    return int(library().lmhead_score_logits_bwd(
+        _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(grad_logp),
+        _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_logits), _stream(stream)))
 
 
 def lmhead_read_device_status(workspace, stream=None):

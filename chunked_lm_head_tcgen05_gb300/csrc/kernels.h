@@ -136,4 +136,14 @@ cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_
                                     cudaStream_t s);
 cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s);
 
+// Logits-level scoring (score_logits.cu).
+cudaError_t launch_score_logits_fwd(const float* logits, const int32_t* targets,
+                                    const uint8_t* mask, int64_t T, int V, float tau, float* logp,
+                                    float* entropy, float* lse, cudaStream_t s);
+cudaError_t launch_score_logits_bwd(const float* logits, const int32_t* targets,
+                                    const uint8_t* mask, int64_t T, int V, float tau,
+                                    const float* grad_logp, const float* grad_entropy,
+                                    const float* lse, const float* entropy, float* d_logits,
+                                    cudaStream_t s);
+
 }  // namespace lmh

@@ -767,6 +767,43 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
   return LMHEAD_OK;
 }
 
+lmhead_status lmhead_score_logits_fwd(const float* logits, const int32_t* targets,
+                                      const uint8_t* loss_mask, int64_t T, int32_t V,
+                                      float temperature, float* logp, float* entropy, float* lse,
+                                      lmhead_stream_t stream) {
+  if (T < 0 || V <= 0 || !std::isfinite(temperature) || !(temperature > 0.f))
+    return LMHEAD_ERR_INVALID_ARG;
+  if (T >= (int64_t{1} << 31)) return LMHEAD_ERR_UNSUPPORTED;
+  if (T == 0) return LMHEAD_OK;
+  if (!logits || !targets || !logp || !lse) return LMHEAD_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LMH_TRY(launch("score_logits_fwd", s, [&] {
+    return launch_score_logits_fwd(logits, targets, loss_mask, T, V, temperature, logp, entropy,
+                                   lse, s);
+  }));
+  return LMHEAD_OK;
+}
+
+lmhead_status lmhead_score_logits_bwd(const float* logits, const int32_t* targets,
+                                      const uint8_t* loss_mask, int64_t T, int32_t V,
+                                      float temperature, const float* grad_logp,
+                                      const float* grad_entropy, const float* lse,
+                                      const float* entropy, float* d_logits,
+                                      lmhead_stream_t stream) {
+  if (T < 0 || V <= 0 || !std::isfinite(temperature) || !(temperature > 0.f))
+    return LMHEAD_ERR_INVALID_ARG;
+  if (T >= (int64_t{1} << 31)) return LMHEAD_ERR_UNSUPPORTED;
+  if (T == 0) return LMHEAD_OK;
+  if (!logits || !targets || !lse || !d_logits || (grad_entropy && !entropy))
+    return LMHEAD_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LMH_TRY(launch("score_logits_bwd", s, [&] {
+    return launch_score_logits_bwd(logits, targets, loss_mask, T, V, temperature, grad_logp,
+                                   grad_entropy, lse, entropy, d_logits, s);
+  }));
+  return LMHEAD_OK;
+}
+
 lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream) {
   if (!workspace) return LMHEAD_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

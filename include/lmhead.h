@@ -195,6 +195,43 @@ int lmhead_fwd_bwd_keeps_logits(int64_t T, int32_t H, int32_t V, int32_t chunk_s
                                 int32_t* block_tokens);
 
 /*
+ * Logits-level scoring, for callers that already hold one chunk's logits
+ * (the per-chunk cross-entropy of a chunked trainer; "Long Sequences (SeCO)"
+ * guide, section "Efficiency").  logits [T, V] fp32 row-major; the scored
+ * logits are z = logits / temperature.  Outputs as lmhead_logps_fwd.
+ *
+ * Non-finite logits (the pages test fused scoring on inf, -inf and NaN
+ * logits and on a row with no finite logit, and require an isfinite mask in
+ * the cotangent -- tunix PR #2913, FusedScoringTest -- without printing
+ * values; this is the reading implemented):
+ *  - a -inf entry has probability 0 and contributes nothing; a -inf target
+ *    logit gives logp = -inf;
+ *  - a NaN or +inf entry anywhere in a row makes its lse, logp and entropy NaN;
+ *  - a row with no finite entry has lse = -inf and NaN logp and entropy.
+ * Unscored rows give +0.0; an id outside [-V, V) gives logp = NaN (there is
+ * no device status word for these calls).  HBM-bound: one read of the logits.
+ */
+lmhead_status lmhead_score_logits_fwd(const float* logits, const int32_t* targets,
+                                      const uint8_t* loss_mask, int64_t T, int32_t V,
+                                      float temperature, float* logp, float* entropy, float* lse,
+                                      lmhead_stream_t stream);
+
+/*
+ * d_logits [T, V] fp32 (overwritten; may be the logits buffer itself) =
+ * d loss / d logits for cotangents grad_logp / grad_entropy (NULL = zero;
+ * entropy required with grad_entropy), given lse (and entropy) from
+ * lmhead_score_logits_fwd.  Non-finite logits get a zero cotangent
+ * (isfinite mask); finite entries of a NaN row get NaN; unscored rows get
+ * zeros.  HBM-bound: one read and one write of [T, V].
+ */
+lmhead_status lmhead_score_logits_bwd(const float* logits, const int32_t* targets,
+                                      const uint8_t* loss_mask, int64_t T, int32_t V,
+                                      float temperature, const float* grad_logp,
+                                      const float* grad_entropy, const float* lse,
+                                      const float* entropy, float* d_logits,
+                                      lmhead_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device status word that the last
  * call using `workspace` left (LMHEAD_OK, LMHEAD_ERR_BAD_TARGET or
  * LMHEAD_ERR_DEVICE_TIMEOUT), or LMHEAD_ERR_CUDA if the read failed.
