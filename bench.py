@@ -135,10 +135,11 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the sources that define the tensor-core GEMM kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_lm_head_tcgen05_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f in ("tc_gemm.cuh", "ptx.cuh", "kernels.h") or (f.startswith("gemm_") and f.endswith(".cu")):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -5,6 +5,7 @@
 // forward; one read and one write backward.  One CTA per row, 16-byte loads
 // when the row layout allows them.
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <cuda_runtime.h>
 
@@ -13,7 +14,8 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kUnroll = 4;   // 16-byte loads in flight per thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -28,24 +30,33 @@ struct Stats {
   int bad;          // saw NaN or +inf
 };
 
-__device__ __forceinline__ void stats_add(Stats& st, float x, float scale) {
-  if (isnan(x) || x == INFINITY) {
-    st.bad = 1;
-    return;
+// Fold n values into the running statistics: one max over the chunk, then
+// the exponentials against it.  NaN / +inf set `bad`; -inf is skipped.
+template <int N>
+__device__ __forceinline__ void stats_add_chunk(Stats& st, const float (&x)[N], float scale) {
+  float cmax = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    if (isnan(x[j]) || x[j] == INFINITY) st.bad = 1;
+    else cmax = fmaxf(cmax, x[j]);
   }
-  if (x == -INFINITY) return;
-  const float u = x * scale;
-  if (u > st.m) {
-    const float dm = st.m - u;   // -inf on the first finite entry
-    const float r = exp2f(dm);
+  const float cm = cmax * scale;
+  if (cm > st.m) {
+    const float dm = st.m - cm;   // -inf on the first finite entry
+    const float r = lmh::ex2_approx(dm);
     st.s1 = st.s > 0.f ? r * fmaf(dm, st.s, st.s1) : 0.f;
     st.s *= r;
-    st.m = u;
+    st.m = cm;
   }
-  const float d = u - st.m;
-  const float e = exp2f(d);
-  st.s += e;
-  st.s1 = fmaf(e, d, st.s1);
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    if (x[j] > -INFINITY && x[j] < INFINITY) {
+      const float d = fmaf(x[j], scale, -st.m);
+      const float e = lmh::ex2_approx(d);
+      st.s += e;
+      st.s1 = fmaf(e, d, st.s1);
+    }
+  }
 }
 
 __device__ __forceinline__ Stats stats_merge(Stats a, Stats b) {
@@ -89,15 +100,30 @@ __global__ void __launch_bounds__(kThreads)
     Stats st{-INFINITY, 0.f, 0.f, 0};
     if (vec4) {
       const float4* r4 = reinterpret_cast<const float4*>(row);
-      for (int i = threadIdx.x; i < V / 4; i += kThreads) {
+      const int n4 = V / 4;
+      int i = threadIdx.x;
+      for (; i + (kUnroll - 1) * kThreads < n4; i += kUnroll * kThreads) {
+        float x[4 * kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          const float4 q = r4[i + k * kThreads];
+          x[4 * k] = q.x;
+          x[4 * k + 1] = q.y;
+          x[4 * k + 2] = q.z;
+          x[4 * k + 3] = q.w;
+        }
+        stats_add_chunk(st, x, scale);
+      }
+      for (; i < n4; i += kThreads) {
         const float4 q = r4[i];
-        stats_add(st, q.x, scale);
-        stats_add(st, q.y, scale);
-        stats_add(st, q.z, scale);
-        stats_add(st, q.w, scale);
+        const float x[4] = {q.x, q.y, q.z, q.w};
+        stats_add_chunk(st, x, scale);
       }
     } else {
-      for (int i = threadIdx.x; i < V; i += kThreads) stats_add(st, row[i], scale);
+      for (int i = threadIdx.x; i < V; i += kThreads) {
+        const float x[1] = {row[i]};
+        stats_add_chunk(st, x, scale);
+      }
     }
     if (threadIdx.x == 0) zy_s = y >= 0 ? row[y] * scale : __int_as_float(0x7fc00000);
 #pragma unroll
@@ -138,7 +164,7 @@ __device__ __forceinline__ float cotangent(float x, float scale, float lse_u, fl
                                            float c1, bool is_target) {
   if (!isfinite(x)) return 0.f;   // isfinite mask
   const float d = fmaf(x, scale, -lse_u);
-  const float p = exp2f(d);
+  const float p = lmh::ex2_approx(d);
   float g = -p * fmaf(a, d, b);
   if (is_target) g += c1;
   return g;
@@ -175,7 +201,24 @@ __global__ void __launch_bounds__(kThreads)
     if (vec4) {
       const float4* r4 = reinterpret_cast<const float4*>(row);
       float4* o4 = reinterpret_cast<float4*>(out);
-      for (int i = threadIdx.x; i < V / 4; i += kThreads) {
+      const int n4 = V / 4;
+      int i = threadIdx.x;
+      for (; i + (kUnroll - 1) * kThreads < n4; i += kUnroll * kThreads) {
+        float4 q[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) q[k] = r4[i + k * kThreads];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          const int c = 4 * (i + k * kThreads);
+          float4 g;
+          g.x = cotangent(q[k].x, scale, lse_u, a, b, c1, c == y);
+          g.y = cotangent(q[k].y, scale, lse_u, a, b, c1, c + 1 == y);
+          g.z = cotangent(q[k].z, scale, lse_u, a, b, c1, c + 2 == y);
+          g.w = cotangent(q[k].w, scale, lse_u, a, b, c1, c + 3 == y);
+          o4[i + k * kThreads] = g;
+        }
+      }
+      for (; i < n4; i += kThreads) {
         const float4 q = r4[i];
         const int c = 4 * i;
         float4 g;
@@ -197,7 +240,7 @@ int grid_rows(int64_t T) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 152;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  const int64_t cap = static_cast<int64_t>(sms) * 4;
   return static_cast<int>(T < cap ? T : cap);
 }
 
