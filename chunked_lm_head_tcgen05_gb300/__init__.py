@@ -23,6 +23,7 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES", "lmhead_logps_fwd_bwd", "lmhead_fwd_bwd_keeps_logits",
     "LMHEAD_OP_FWD_BWD", "LMHEAD_STRATEGY_AUTO", "LMHEAD_STRATEGY_RECOMPUTE",
     "LMHEAD_STRATEGY_KEEP_LOGITS", "lmhead_score_logits_fwd", "lmhead_score_logits_bwd",
+    "lmhead_selftest_bounded_wait",
     "forward", "backward",
 ]
 
@@ -73,6 +74,7 @@ _SIGNATURES = {
                                             _VP, ctypes.c_int, ctypes.c_int, _VP, _SZ, _VP]),
     "lmhead_fwd_bwd_keeps_logits": (ctypes.c_int, [_I64, _I32, _I32, _I32,
                                                    ctypes.POINTER(_I32)]),
+    "lmhead_selftest_bounded_wait": (ctypes.c_int, [_VP, _SZ, ctypes.c_uint32, _VP]),
     "lmhead_score_logits_fwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.c_float, _VP,
                                                _VP, _VP, _VP]),
     "lmhead_score_logits_bwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.c_float, _VP,
@@ -273,6 +275,13 @@ def lmhead_score_logits_bwd(logits, targets, loss_mask, temperature, grad_logp, 
     return int(library().lmhead_score_logits_bwd(
         _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(grad_logp),
         _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_logits), _stream(stream)))
+
+
+def lmhead_selftest_bounded_wait(workspace, limit_ms, stream=None):
+    """C ``lmhead_selftest_bounded_wait``; returns the status code of the launch."""
+    return int(library().lmhead_selftest_bounded_wait(
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_ms),
+        _stream(stream)))
 
 
 def lmhead_read_device_status(workspace, stream=None):

@@ -136,6 +136,9 @@ cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_
                                     cudaStream_t s);
 cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s);
 
+// Self-test of the bounded mbarrier wait (selftest.cu).
+cudaError_t launch_bounded_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);
+
 // Logits-level scoring (score_logits.cu).
 cudaError_t launch_score_logits_fwd(const float* logits, const int32_t* targets,
                                     const uint8_t* mask, int64_t T, int V, float tau, float* logp,

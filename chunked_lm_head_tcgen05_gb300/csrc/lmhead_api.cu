@@ -804,6 +804,20 @@ lmhead_status lmhead_score_logits_bwd(const float* logits, const int32_t* target
   return LMHEAD_OK;
 }
 
+lmhead_status lmhead_selftest_bounded_wait(void* workspace, size_t workspace_bytes,
+                                           uint32_t limit_ms, lmhead_stream_t stream) {
+  if (!workspace || workspace_bytes < sizeof(DeviceState) || limit_ms == 0 || limit_ms > 10000)
+    return LMHEAD_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return LMHEAD_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* st = static_cast<DeviceState*>(workspace);
+  LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(st, 0, s); }));
+  LMH_TRY(launch("bounded_wait_selftest", s, [&] {
+    return launch_bounded_wait_selftest(&st->status, uint64_t{limit_ms} * 1000000ull, s);
+  }));
+  return LMHEAD_OK;
+}
+
 lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream) {
   if (!workspace) return LMHEAD_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

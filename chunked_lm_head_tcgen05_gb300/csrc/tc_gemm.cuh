@@ -81,7 +81,7 @@ static_assert(sizeof(SharedCtl) <= 256, "control block exceeds its shared memory
 // (the barrier is also arrived on by the peer CTA).
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                             int* status) {
+                                             int* status, uint64_t limit_ns = WAIT_LIMIT_NS) {
   auto poll = [&]() {
     return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
@@ -92,7 +92,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     for (int i = 0; i < 128; ++i)
       if (poll()) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       atomicCAS(status, 0, STATUS_DEVICE_TIMEOUT);
       return false;

@@ -232,6 +232,19 @@ lmhead_status lmhead_score_logits_bwd(const float* logits, const int32_t* target
                                       lmhead_stream_t stream);
 
 /*
+ * Self-test of failure detection (the pages have no counterpart; the
+ * kernels need it on shared GPUs): launches one CTA that allocates tensor
+ * memory and waits, with the same bounded mbarrier wait every GEMM pipeline
+ * stage uses, on a barrier nothing arrives on.  After `limit_ms` (1..10000)
+ * the wait gives up, LMHEAD_ERR_DEVICE_TIMEOUT is recorded in the workspace's
+ * status word (read it with lmhead_read_device_status), tensor memory is
+ * freed and the kernel exits; the context stays usable.  workspace: at
+ * least 256 bytes, 256-byte aligned.
+ */
+lmhead_status lmhead_selftest_bounded_wait(void* workspace, size_t workspace_bytes,
+                                           uint32_t limit_ms, lmhead_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device status word that the last
  * call using `workspace` left (LMHEAD_OK, LMHEAD_ERR_BAD_TARGET or
  * LMHEAD_ERR_DEVICE_TIMEOUT), or LMHEAD_ERR_CUDA if the read failed.
