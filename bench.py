@@ -371,6 +371,55 @@ def run_ours(args, rank, world, local):
                    "tflops_counted": 6.0 * Tv * H * V * world * max(3, args.steps // 2) / tf / 1e12}
     del ws2
 
+    # ---- forward alone, backward alone, and the logp-only backward (no entropy cotangent)
+    def fwd_only():
+        rc = lm.lmhead_logps_fwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau, c,
+                                 logp, ent, lse, ws, stream)
+        if rc:
+            raise lm.LmheadError(rc, "fwd")
+
+    def bwd_only(grad_entropy=g["grad_entropy"]):
+        rc = lm.lmhead_logps_bwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau, c,
+                                 g["grad_logp"], grad_entropy, lse, ent, dh, dw, 0, ws, stream)
+        if rc:
+            raise lm.LmheadError(rc, "bwd")
+
+    nb = max(3, args.steps // 4)
+    fwd_only()
+    tfw = max_over_ranks(timed(fwd_only, nb), world) / nb
+    bwd_only()
+    tbw = max_over_ranks(timed(bwd_only, nb), world) / nb
+    bwd_only(None)
+    tbl = max_over_ranks(timed(lambda: bwd_only(None), nb), world) / nb
+    fl = Tv * H * V
+    splits, tb_rows, vb_cols = lm.lmhead_plan_info(T, H, V, c)
+    merge = per.get("fwd_merge")
+    merge_bytes = Tv * (16 * splits + 4 + 12 + (4 if g["loss_mask"] is not None else 0))
+    breakdown = {
+        "fwd": {"ms": tfw * 1e3, "tflops": 2.0 * fl / tfw / 1e12},
+        "bwd": {"ms": tbw * 1e3, "tflops_counted": 4.0 * fl / tbw / 1e12,
+                "tflops_executed": 6.0 * fl / tbw / 1e12},
+        "bwd_logp_only": {"ms": tbl * 1e3, "tflops_counted": 4.0 * fl / tbl / 1e12,
+                          "note": "grad_entropy = NULL"},
+        "fwd_merge": {"us": merge[1] / merge[0] * 1e3 if merge else None,
+                      "bytes": merge_bytes,
+                      "gb_per_s": merge_bytes / (merge[1] / merge[0] / 1e3) / 1e9 if merge else None,
+                      "note": "%d vocabulary splits; a few microseconds, launch-latency bound at "
+                              "this size" % splits},
+        "plan": {"fwd_splits": splits, "bwd_tokens": tb_rows, "bwd_vocab": vb_cols},
+    }
+
+    # ---- device memory: the library allocates nothing; its workspace is bounded by the chunk
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step(g)
+    torch.cuda.synchronize()
+    memory = {"workspace_bytes": ws.numel(),
+              "peak_delta_during_step_bytes": torch.cuda.max_memory_allocated(dev) - base,
+              "logits_bytes_bf16": 2 * T * V,
+              "workspace_over_logits": ws.numel() / (2.0 * T * V)}
+
     counted = 6.0 * Tv * H * V
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -392,6 +441,8 @@ def run_ours(args, rank, world, local):
         "single_call_fwd_bwd": single_call,
         "roofline": roofline,
         "kernels": kernels,
+        "breakdown": breakdown,
+        "memory": memory,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)

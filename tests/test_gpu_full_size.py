@@ -105,3 +105,37 @@ def test_single_call_keep_logits_full_size(name):
     e["d_hidden"] = rel_fro(g["d_hidden"][rows], o["d_hidden"])
     assert e["d_weight"] <= LIMITS["d_weight"] and e["d_hidden"] <= LIMITS["d_hidden"], e
     print(name, e)
+
+
+def test_device_memory_bounded_by_chunk(case):
+    """Everything the head adds on the device during a forward + backward (its
+    workspace included) stays below one bf16 [T, V] logits tensor, and the
+    library itself allocates nothing: the peak over the calls equals the
+    allocations made before them."""
+    import chunked_lm_head_tcgen05_gb300 as lm
+    from gpu_helpers import ensure_built, to_device
+    ensure_built()
+    w, x = case
+    g = to_device(x)
+    T, H = g["hidden"].shape
+    V = g["weight"].shape[0]
+    c, tau = x["chunk_size"], x["temperature"]
+    logp, ent, lse = (torch.empty(T, device="cuda") for _ in range(3))
+    dh = torch.empty((T, H), device="cuda")
+    dw = torch.empty((V, H), device="cuda")
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    ws = torch.empty(max(lm.lmhead_workspace_size(0, T, H, V, c),
+                         lm.lmhead_workspace_size(1, T, H, V, c)), dtype=torch.uint8,
+                     device="cuda")
+    after_ws = torch.cuda.memory_allocated()
+    assert lm.lmhead_logps_fwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau, c,
+                               logp, ent, lse, ws) == 0
+    assert lm.lmhead_logps_bwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau, c,
+                               g["grad_logp"], g["grad_entropy"], lse, ent, dh, dw, 0, ws) == 0
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated()
+    assert peak == after_ws, (peak, after_ws)
+    assert peak - base < 2 * T * V, (peak - base, 2 * T * V)
+    assert lm.lmhead_read_device_status(ws) == 0
