@@ -26,6 +26,7 @@ __device__ __forceinline__ int wrap_target(int y, int V) {
 __global__ void clear_state_kernel(DeviceState* st, int rows) {
   st->status = 0;
   st->rows = rows;
+  st->abort_all = 0;
 }
 
 // One CTA: stable compaction of the scored positions (ascending order), the

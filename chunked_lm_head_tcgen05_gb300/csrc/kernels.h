@@ -25,6 +25,7 @@ constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators, double buffered
 // swizzled) that TMA bulk-stores write out.
 constexpr uint32_t STAGING_BYTES = 2 * 16384;
 constexpr size_t GEMM_SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 256 + 1024;
+constexpr size_t BWD_ALL_SMEM_BYTES = GEMM_SMEM_BYTES + 1024;   // + the token-block unit table
 
 // Device status word values (same numbers as the public lmhead_status).
 constexpr int STATUS_DEVICE_TIMEOUT = 5;
@@ -34,7 +35,8 @@ constexpr int STATUS_BAD_TARGET = 6;
 struct DeviceState {
   int status;       // first error seen on the device (0 = none)
   int rows;         // number of scored tokens T_v (written by the compaction step)
-  int pad[62];
+  int abort_all;    // set by a persistent kernel's CTA that gave up, so the others stop too
+  int pad[61];
 };
 
 enum EpiKind : int {
@@ -88,7 +90,9 @@ constexpr int MAX_PROBLEMS = 2;
 
 struct Problem {
   GemmArgs p;
-  int a_mn;   // 1: the A operand is MN-major in memory (B majorness is a template flag)
+  int a_mn;   // 1: the A operand is MN-major in memory (B majorness is a template flag).
+              // MN-major operands take 3-D maps (64 elements, K rows, 64-element
+              // chunks) with boxes of 64 x 64 x (rows per CTA / 64).
 };
 
 struct LaunchArgs {
@@ -100,7 +104,40 @@ struct LaunchArgs {
   int* counter;
 };
 
+// The whole backward in one persistent launch on CTA pairs: the dz, dh and
+// dW tiles of every backward block in one dynamically fetched sequence,
+// ordered by per-tile completion flags instead of launch boundaries.  Blocks
+// (token block tb, vocabulary block vb) are numbered b = tb * n_vb + vb; T_b
+// and V_b are multiples of 256.  Per block the units are its dz tiles (column
+// major), its dh tiles (row major) and its dW tiles (vocabulary-tile major).
+// The first unit of each token block is kept in shared memory (1 KB).
+constexpr int BWD_ALL_MAX_TOKEN_BLOCKS = 255;
+
+struct BwdAllArgs {
+  CUtensorMap h_k;     // hidden rows [rows, H], K-major, boxes 64 x 128: A of dz
+  CUtensorMap w_k;     // W [V, H], K-major, boxes 64 x 128: B of dz (half of N per CTA)
+  CUtensorMap dz_k;    // dz scratch [T_b, V_b], boxes 64 x 128: dz tile stores and A of dh
+  CUtensorMap w_mn;    // W as (64, V rows, H / 64 chunks), boxes 64 x 64 x 2: MN-major B of dh
+  CUtensorMap dz_mn;   // dz scratch as (64, T_b rows, V_b / 64 chunks), boxes 64 x 64 x 2: A of dW
+  CUtensorMap h_mn;    // hidden rows as (64, rows, H / 64 chunks), boxes 64 x 64 x 2: B of dW
+  CUtensorMap dh_out;  // d_hidden fp32 [T, H], boxes 32 x 128 (when rows are not scattered)
+  CUtensorMap dw_out;  // d_weight fp32 [V, H], boxes 32 x 128
+  int T_b, V_b, n_tb, n_vb, V, H, T_alloc;
+  int MT, NT;          // T_b / 256 and V_b / 256: flags per block and kind
+  DeviceState* st;     // scored count, status word, abort word
+  float scale;         // log2(e) / tau
+  const int* y_c;
+  const float4* coef;
+  const int* row_map;  // compaction index (d_hidden rows scattered), or NULL
+  float* d_hidden;
+  float* d_weight;
+  int accumulate_dweight;
+  int* unit_counter;
+  int* flags;          // per block: all dz [1], dz columns [NT], dh rows [MT], dW columns [NT]
+};
+
 // Launchers.  Each returns the launch error (cudaSuccess when enqueued).
+cudaError_t launch_gemm_bwd_all(const BwdAllArgs& a, int grid, cudaStream_t s);
 // pair = true runs each tile on a cluster of two CTAs (tcgen05 cta_group::2,
 // 256-row units, B staged half per CTA); the B maps must then use 128-row
 // K-major boxes.  `grid` is the number of CTAs wanted.

@@ -93,6 +93,16 @@ bool use_pair() {
   return on;
 }
 
+// The backward runs as two launches per block; LMHEAD_BWD_PERSISTENT=1 in
+// the environment selects the single persistent launch instead (same bits,
+// measured slower on GB300: its tiles start staggered, so tiles sharing W
+// and dz slices no longer walk K together and more operands come from DRAM).
+// Read on every call so that both paths can be compared in one process.
+bool use_bwd_persistent() {
+  const char* e = std::getenv("LMHEAD_BWD_PERSISTENT");
+  return e && e[0] == '1';
+}
+
 int unit_rows() { return use_pair() ? 2 * BM : BM; }
 uint32_t b_box_rows() { return use_pair() ? BN / 2 : BN; }
 
@@ -123,6 +133,26 @@ bool make_map_typed(CUtensorMap* m, CUtensorMapDataType type, const void* base, 
   cuuint32_t es[2] = {1, 1};
   return enc(m, type, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major bf16 operand map: the matrix [rows][inner] (rows `row_bytes`
+// apart, K along the rows) viewed as 64-element chunks, (64, rows,
+// ceil(inner / 64)), the chunks 128 bytes apart.  A box of 64 x 64 x `chunks`
+// lands in shared memory as `chunks` swizzled 64 x 64 images 8 KB apart: one
+// instruction per K step instead of one per chunk.  Rows past `rows` read as
+// zero; a partial last chunk reads the row's padding (callers discard those
+// M rows, or the row is padded with zeros).
+bool make_map_mn(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t row_bytes, uint32_t chunks) {
+  auto enc = encode_fn();
+  if (!enc || inner == 0 || rows == 0) return false;
+  cuuint64_t dims[3] = {64, rows, (inner + 63) / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -192,15 +222,18 @@ struct BwdPlan {
 // Backward blocks T_b x V_b with T_b * V_b <= chunk_size * V (the scratch
 // bound); T_b ~ V_b ~ sqrt(chunk_size * V) minimises the fp32
 // read-modify-write traffic of dh and dW, 8 T V H (1/T_b + 1/V_b) bytes.
+// T_b is a multiple of 256 rows (one CTA pair's tile), V_b of 256 columns.
 BwdPlan plan_bwd(int64_t T, int64_t V, int64_t chunk) {
   BwdPlan p;
+  constexpr int64_t TU = 2 * BM;
   const int64_t T_alloc = round_up(T, BM);
   const int64_t V_pad = round_up(V, BN);
   const double S = static_cast<double>(chunk) * static_cast<double>(V);
-  int64_t tb_max = static_cast<int64_t>(std::floor(std::sqrt(S) / BM)) * BM;
-  tb_max = std::max<int64_t>(BM, std::min<int64_t>(tb_max, T_alloc));
+  int64_t tb_max = static_cast<int64_t>(std::floor(std::sqrt(S) / TU)) * TU;
+  tb_max = std::max<int64_t>(TU, std::min<int64_t>(tb_max, round_up(T_alloc, TU)));
   p.n_tb = ceil_div(T_alloc, tb_max);
-  p.Tb = round_up(ceil_div(T_alloc, p.n_tb), BM);
+  p.Tb = round_up(ceil_div(T_alloc, p.n_tb), TU);
+  p.n_tb = ceil_div(T_alloc, p.Tb);
   int64_t vb_max = static_cast<int64_t>(std::floor(S / static_cast<double>(p.Tb) / BN)) * BN;
   vb_max = std::max<int64_t>(BN, std::min<int64_t>(vb_max, V_pad));
   p.n_vb = ceil_div(V_pad, vb_max);
@@ -260,8 +293,11 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
   if (op == LMHEAD_OP_FWD) {
     L.n_counters = 1;
   } else if (op == LMHEAD_OP_BWD) {
+    // two unit counters per block (per-block launches), or one counter and
+    // the tile completion flags of the persistent launch
     const BwdPlan bp = plan_bwd(T, V, chunk);
-    L.n_counters = 2 * bp.n_tb * bp.n_vb;
+    const int64_t blocks = bp.n_tb * bp.n_vb;
+    L.n_counters = std::max<int64_t>(2 * blocks, 1 + blocks * (1 + bp.Tb / (2 * BM) + 2 * bp.Vb / BN));
   } else {
     L.n_counters = 2 * plan_fused(T, H, V, chunk).n_tb;
   }
@@ -495,6 +531,44 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   const bool pair = use_pair();
   const int64_t um = unit_rows();
   const int64_t ctas = pair ? 2 : 1;
+
+  if (pair && use_bwd_persistent() && bp.n_tb <= BWD_ALL_MAX_TOKEN_BLOCKS) {
+    // every block's dz, dh and dW tiles in one launch, ordered by tile flags
+    BwdAllArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const uint64_t Tb = static_cast<uint64_t>(bp.Tb), Vb = static_cast<uint64_t>(bp.Vb);
+    if (!make_map(&a.h_k, f.h_src, H, f.rows_avail, 2ull * H, BK, BM) ||
+        !make_map(&a.w_k, weight, H, V, 2ull * H, BK, BN / 2) ||
+        !make_map(&a.dz_k, dz, Vb, Tb, 2ull * Vb, 64, BM) ||
+        !make_map_mn(&a.w_mn, weight, H, V, 2ull * H, 2) ||
+        !make_map_mn(&a.dz_mn, dz, Vb, Tb, 2ull * Vb, 2) ||
+        !make_map_mn(&a.h_mn, f.h_src, H, f.rows_avail, 2ull * H, 2) ||
+        (!f.idx && !make_out_map_f32(&a.dh_out, d_hidden, H, T, H)) ||
+        !make_out_map_f32(&a.dw_out, d_weight, H, V, H))
+      return LMHEAD_ERR_CUDA;
+    a.T_b = static_cast<int>(bp.Tb);
+    a.V_b = static_cast<int>(bp.Vb);
+    a.n_tb = static_cast<int>(bp.n_tb);
+    a.n_vb = static_cast<int>(bp.n_vb);
+    a.V = V;
+    a.H = H;
+    a.T_alloc = static_cast<int>(f.T_alloc);
+    a.MT = static_cast<int>(bp.Tb / (2 * BM));
+    a.NT = static_cast<int>(bp.Vb / BN);
+    a.st = f.st;
+    a.scale = scale;
+    a.y_c = f.y_c;
+    a.coef = coef;
+    a.row_map = f.idx;
+    a.d_hidden = d_hidden;
+    a.d_weight = d_weight;
+    a.accumulate_dweight = accumulate_dweight ? 1 : 0;
+    a.unit_counter = f.counters;
+    a.flags = f.counters + 1;
+    LMH_TRY(launch("bwd_all_gemm", s, [&] { return launch_gemm_bwd_all(a, sms, s); }));
+    return LMHEAD_OK;
+  }
+
   for (int64_t tb = 0; tb < bp.n_tb; ++tb) {
     const int64_t t0 = tb * bp.Tb;
     if (t0 >= f.T_alloc) break;
@@ -541,7 +615,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       std::memset(&lg, 0, sizeof(lg));
       // problem 0: dh[block rows] (+)= dz . W_block   (K = vocabulary of the block)
       if (!make_map(&lg.map_a[0], dz, vact, m_cap, 2ull * bp.Vb, BK, BM)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&lg.map_b[0], w_blk, H, vact, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+      if (!make_map_mn(&lg.map_b[0], w_blk, H, vact, 2ull * H, b_box_rows() / 64))
+        return LMHEAD_ERR_CUDA;
       GemmArgs& ph = lg.prob[0].p;
       lg.prob[0].a_mn = 0;
       ph.m_cap = static_cast<int>(m_cap);
@@ -565,8 +640,9 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
           return LMHEAD_ERR_CUDA;
       }
       // problem 1: dW[block vocab rows] (+)= dz^T . h_block (K = tokens, ascending blocks)
-      if (!make_map(&lg.map_a[1], dz, vact, m_cap, 2ull * bp.Vb, 64, 64)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+      if (!make_map_mn(&lg.map_a[1], dz, vact, m_cap, 2ull * bp.Vb, BM / 64) ||
+          !make_map_mn(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, b_box_rows() / 64))
+        return LMHEAD_ERR_CUDA;
       GemmArgs& pw = lg.prob[1].p;
       lg.prob[1].a_mn = 1;
       pw.m_cap = static_cast<int>(vact);
@@ -718,7 +794,8 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
     LaunchArgs lg;
     std::memset(&lg, 0, sizeof(lg));
     if (!make_map(&lg.map_a[0], zbuf, V, m_cap, 2ull * fp.V_pad, BK, BM)) return LMHEAD_ERR_CUDA;
-    if (!make_map(&lg.map_b[0], weight, H, V, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+    if (!make_map_mn(&lg.map_b[0], weight, H, V, 2ull * H, b_box_rows() / 64))
+      return LMHEAD_ERR_CUDA;
     GemmArgs& ph = lg.prob[0].p;
     lg.prob[0].a_mn = 0;
     ph.m_cap = static_cast<int>(m_cap);
@@ -740,8 +817,9 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
                             std::min<int64_t>(m_cap, T - t0), H))
         return LMHEAD_ERR_CUDA;
     }
-    if (!make_map(&lg.map_a[1], zbuf, V, m_cap, 2ull * fp.V_pad, 64, 64)) return LMHEAD_ERR_CUDA;
-    if (!make_map(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, 64, 64)) return LMHEAD_ERR_CUDA;
+    if (!make_map_mn(&lg.map_a[1], zbuf, V, m_cap, 2ull * fp.V_pad, BM / 64) ||
+        !make_map_mn(&lg.map_b[1], h_blk, H, h_rows, 2ull * H, b_box_rows() / 64))
+      return LMHEAD_ERR_CUDA;
     GemmArgs& pw = lg.prob[1].p;
     lg.prob[1].a_mn = 1;
     pw.m_cap = V;

@@ -47,6 +47,9 @@ namespace lmh {
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int SCHED_DEPTH = 4;
 constexpr int MAX_STAGES = 6;
+// The next unit's index is fetched this many K steps before the current
+// unit's last load, so that the fetch's latency is hidden behind the loads.
+constexpr int FETCH_AHEAD_KB = 8;
 
 template <bool PAIR>
 struct TileCfg {
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_par = 0;
       bool ok = true;
+      int ahead = -1;   // unit index fetched ahead, -1 = none
       for (int i = 0; ok; ++i) {
         const int slot = i & (SCHED_DEPTH - 1);
         const uint32_t spar = (i / SCHED_DEPTH) & 1;
@@ -279,7 +283,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          u = atomicAdd(L.counter, 1);
+          u = ahead >= 0 ? ahead : atomicAdd(L.counter, 1);
+          ahead = -1;
           if (u >= total_units) u = -1;
           ctl->sched[slot] = u;
           if constexpr (PAIR) {
@@ -308,6 +313,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int n = nb; ok && n < ne; ++n) {
           const int bcol = n * BN + static_cast<int>(rank) * C::B_ROWS;
           for (int kb = 0; kb < s.k_blocks; ++kb) {
+            if (leader && ahead < 0 && n == ne - 1 && kb == max(0, s.k_blocks - FETCH_AHEAD_KB))
+              ahead = atomicAdd(L.counter, 1);
             if (!wait_bounded<PAIR>(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
               ok = false;
               break;
@@ -316,35 +323,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * C::CTAS);
             const uint32_t sa = smem_base + stage * C::STAGE;
             const uint32_t sb = sa + A_TILE_BYTES;
+            // MN-major operands use 3-D maps (64 elements, K rows, 64-element
+            // chunks): one instruction loads all of this CTA's chunks
             if constexpr (PAIR) {
               const uint32_t fb = map_to_cta(fb_local, 0);
-              if (!a_mn) {
+              if (!a_mn)
                 tma_load_2d_pair(sa, ma, fb, kb * BK, arow);
-              } else {
-                tma_load_2d_pair(sa, ma, fb, arow, kb * BK);
-                tma_load_2d_pair(sa + 8192, ma, fb, arow + 64, kb * BK);
-              }
-              if (!B_MN) {
+              else
+                tma_load_3d_pair(sa, ma, fb, 0, kb * BK, arow / 64);
+              if (!B_MN)
                 tma_load_2d_pair(sb, mb, fb, kb * BK, bcol);
-              } else {
-#pragma unroll
-                for (int j = 0; j < C::B_ROWS / 64; ++j)
-                  tma_load_2d_pair(sb + j * 8192, mb, fb, bcol + 64 * j, kb * BK);
-              }
+              else
+                tma_load_3d_pair(sb, mb, fb, 0, kb * BK, bcol / 64);
             } else {
-              if (!a_mn) {
+              if (!a_mn)
                 tma_load_2d(sa, ma, fb_local, kb * BK, arow);
-              } else {
-                tma_load_2d(sa, ma, fb_local, arow, kb * BK);
-                tma_load_2d(sa + 8192, ma, fb_local, arow + 64, kb * BK);
-              }
-              if (!B_MN) {
+              else
+                tma_load_3d(sa, ma, fb_local, 0, kb * BK, arow / 64);
+              if (!B_MN)
                 tma_load_2d(sb, mb, fb_local, kb * BK, bcol);
-              } else {
-#pragma unroll
-                for (int j = 0; j < C::B_ROWS / 64; ++j)
-                  tma_load_2d(sb + j * 8192, mb, fb_local, bcol + 64 * j, kb * BK);
-              }
+              else
+                tma_load_3d(sb, mb, fb_local, 0, kb * BK, bcol / 64);
             }
             issued_mask |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);

@@ -170,6 +170,7 @@ def test_plan_is_chunk_bounded(lib):
     for T, V, c in [(4096, 151936, 512), (65536, 151936, 512), (65536, 151936, 4096),
                     (200000, 151936, 4096), (256, 2048, 64), (300, 3001, 16), (5, 7, 1)]:
         _, tb, vb = lm.lmhead_plan_info(T, 128, V, c)
-        assert tb % 128 == 0 and vb % 256 == 0
-        assert tb * vb <= max(c * V, 128 * 256) + 128 * 256 + 256 * tb + 128 * vb, (T, V, c, tb, vb)
-        assert tb <= (T + 127) // 128 * 128
+        # token blocks are whole 256-row pair tiles
+        assert tb % 256 == 0 and vb % 256 == 0
+        assert tb * vb <= max(c * V, 256 * 256) + 256 * 256 + 256 * tb + 256 * vb, (T, V, c, tb, vb)
+        assert tb <= (T + 255) // 256 * 256

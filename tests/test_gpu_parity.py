@@ -179,6 +179,8 @@ def test_instrumentation_counts_and_names():
     n = lm.lmhead_profile_count()
     names = [lm.lmhead_profile_record(i)[0] for i in range(n)]
     assert lm.lmhead_launch_count() - n0 == n
-    for k in ("fwd_stats_gemm", "fwd_merge", "bwd_dz_gemm", "bwd_grad_gemm"):
+    for k in ("fwd_stats_gemm", "fwd_merge", "bwd_prep"):
         assert k in names
+    # the backward GEMMs: one persistent launch, or two launches per block
+    assert "bwd_all_gemm" in names or ("bwd_dz_gemm" in names and "bwd_grad_gemm" in names)
     assert all(lm.lmhead_profile_record(i)[1] >= 0 for i in range(n))
