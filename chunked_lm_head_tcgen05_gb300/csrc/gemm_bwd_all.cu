@@ -236,7 +236,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tb_prefix[A.n_tb] = acc;
   }
   __syncthreads();
-  const int total_units = tb_prefix[A.n_tb];
+  // This launch's units: all of them, or one window (see BwdAllArgs::window).
+  int unit_begin = 0, unit_end = tb_prefix[A.n_tb];
+  if (A.window >= 0) {
+    const int n_blocks = A.n_tb * A.n_vb;
+    auto first_dh = [&](int b) {   // number of the first dh unit of block b
+      const int tb = b / A.n_vb, vb = b - tb * A.n_vb;
+      const Blk k0 = block_of(A, tb, 0, scored);
+      const Blk k = block_of(A, tb, vb, scored);
+      return tb_prefix[tb] + vb * units_full(A, k0.mt, ht) + k.mt * k.nt;
+    };
+    if (A.window > 0) unit_begin = first_dh(A.window - 1);
+    if (A.window < n_blocks) unit_end = first_dh(A.window);
+  }
 
   auto sched_take = [&](int slot, uint32_t spar, int& u) -> bool {
     if (!wait_bar(smem_addr(&ctl->sfull[slot]), spar, abort, st)) return false;
@@ -271,9 +283,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          u = ahead >= 0 ? ahead : atomicAdd(A.unit_counter, 1);
+          u = unit_begin + (ahead >= 0 ? ahead : atomicAdd(A.unit_counter, 1));
           ahead = -1;
-          if (u >= total_units) u = -1;
+          if (u >= unit_end) u = -1;
           ctl->sched[slot] = u;
           st_shared_remote(map_to_cta(smem_addr(&ctl->sched[slot]), 1), u);
           mbar_arrive_remote(map_to_cta(smem_addr(&ctl->sfull[slot]), 1));

@@ -132,8 +132,15 @@ struct BwdAllArgs {
   float* d_hidden;
   float* d_weight;
   int accumulate_dweight;
-  int* unit_counter;
+  int* unit_counter;   // zeroed; one per launch
   int* flags;          // per block: all dz [1], dz columns [NT], dh rows [MT], dW columns [NT]
+  // -1: every unit in one launch.  w in [0, blocks]: launch w of a sequence of
+  // blocks + 1 launches runs the units from block w-1's first dh tile up to
+  // block w's first dh tile (launch 0: block 0's dz tiles; the last: the
+  // last block's dh and dW tiles), so each launch starts with one block's
+  // gradient tiles on every SM together and ends with the next block's dz
+  // tiles filling its tail.
+  int window;
 };
 
 // Launchers.  Each returns the launch error (cudaSuccess when enqueued).

@@ -93,14 +93,18 @@ bool use_pair() {
   return on;
 }
 
-// The backward runs as two launches per block; LMHEAD_BWD_PERSISTENT=1 in
-// the environment selects the single persistent launch instead (same bits,
-// measured slower on GB300: its tiles start staggered, so tiles sharing W
-// and dz slices no longer walk K together and more operands come from DRAM).
-// Read on every call so that both paths can be compared in one process.
-bool use_bwd_persistent() {
+// Backward launch structure, from LMHEAD_BWD_PERSISTENT (read on every call
+// so that the forms can be compared in one process; all give the same bits):
+//   0  two launches per block (dz, then dh + dW);
+//   1  one persistent launch for all blocks (measured slower on GB300: its
+//      tiles start staggered, so tiles sharing W and dz slices no longer walk
+//      K together and more operands come from DRAM);
+//   2  windows: blocks + 1 launches, each a block's dh + dW tiles followed by
+//      the next block's dz tiles, ordered by tile flags.
+int bwd_mode() {
   const char* e = std::getenv("LMHEAD_BWD_PERSISTENT");
-  return e && e[0] == '1';
+  if (!e || !e[0]) return 0;
+  return e[0] == '1' ? 1 : (e[0] == '2' ? 2 : 0);
 }
 
 int unit_rows() { return use_pair() ? 2 * BM : BM; }
@@ -297,7 +301,8 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
     // the tile completion flags of the persistent launch
     const BwdPlan bp = plan_bwd(T, V, chunk);
     const int64_t blocks = bp.n_tb * bp.n_vb;
-    L.n_counters = std::max<int64_t>(2 * blocks, 1 + blocks * (1 + bp.Tb / (2 * BM) + 2 * bp.Vb / BN));
+    L.n_counters =
+        std::max<int64_t>(2 * blocks, (blocks + 1) + blocks * (1 + bp.Tb / (2 * BM) + 2 * bp.Vb / BN));
   } else {
     L.n_counters = 2 * plan_fused(T, H, V, chunk).n_tb;
   }
@@ -532,7 +537,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   const int64_t um = unit_rows();
   const int64_t ctas = pair ? 2 : 1;
 
-  if (pair && use_bwd_persistent() && bp.n_tb <= BWD_ALL_MAX_TOKEN_BLOCKS) {
+  const int mode = bwd_mode();
+  if (pair && mode != 0 && bp.n_tb <= BWD_ALL_MAX_TOKEN_BLOCKS) {
     // every block's dz, dh and dW tiles in one launch, ordered by tile flags
     BwdAllArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -563,9 +569,19 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
     a.d_hidden = d_hidden;
     a.d_weight = d_weight;
     a.accumulate_dweight = accumulate_dweight ? 1 : 0;
-    a.unit_counter = f.counters;
-    a.flags = f.counters + 1;
-    LMH_TRY(launch("bwd_all_gemm", s, [&] { return launch_gemm_bwd_all(a, sms, s); }));
+    const int blocks = static_cast<int>(bp.n_tb * bp.n_vb);
+    a.flags = f.counters + (blocks + 1);
+    if (mode == 1) {
+      a.window = -1;
+      a.unit_counter = f.counters;
+      LMH_TRY(launch("bwd_all_gemm", s, [&] { return launch_gemm_bwd_all(a, sms, s); }));
+    } else {
+      for (int w = 0; w <= blocks; ++w) {
+        a.window = w;
+        a.unit_counter = f.counters + w;
+        LMH_TRY(launch("bwd_window_gemm", s, [&] { return launch_gemm_bwd_all(a, sms, s); }));
+      }
+    }
     return LMHEAD_OK;
   }
 

@@ -1,6 +1,8 @@
 """The backward as one persistent launch (tile completion flags between the dz,
-dh and dW tiles of all blocks) against the per-block path (two launches per
-block, ordered by the stream), selected with LMHEAD_BWD_PERSISTENT.
+dh and dW tiles of all blocks), and as windowed launches (one block's dh and
+dW tiles then the next block's dz tiles per launch), against the per-block
+path (two launches per block, ordered by the stream), selected with
+LMHEAD_BWD_PERSISTENT = 1, 2 and 0.
 
 Both compute every tile from the same operands in the same order, so the
 gradients must agree bit for bit; each case is also held to the oracle.
@@ -40,22 +42,29 @@ def _kernels(fn):
     return out, names
 
 
+KERNEL = {"0": "bwd_dz_gemm", "1": "bwd_all_gemm", "2": "bwd_window_gemm"}
+
+
 def _both(x, **kw):
+    """Per-block path, then the persistent launch, then the windowed launches:
+    returns (per-block result, persistent result) after checking that the
+    windowed result has the persistent result's bits."""
     old = os.environ.get("LMHEAD_BWD_PERSISTENT")
+    out = {}
     try:
-        os.environ["LMHEAD_BWD_PERSISTENT"] = "0"
-        a, na = _kernels(lambda: run_gpu(x, **kw))
-        os.environ["LMHEAD_BWD_PERSISTENT"] = "1"
-        b, nb = _kernels(lambda: run_gpu(x, **kw))
-        # the two runs really took different paths
-        assert "bwd_dz_gemm" in na and "bwd_all_gemm" not in na, na
-        assert "bwd_all_gemm" in nb and "bwd_dz_gemm" not in nb, nb
+        for mode in ("0", "1", "2"):
+            os.environ["LMHEAD_BWD_PERSISTENT"] = mode
+            out[mode], names = _kernels(lambda: run_gpu(x, **kw))
+            # each run really took its own path
+            assert KERNEL[mode] in names, (mode, names)
+            assert not any(KERNEL[m] in names for m in KERNEL if m != mode), (mode, names)
     finally:
         if old is None:
             os.environ.pop("LMHEAD_BWD_PERSISTENT", None)
         else:
             os.environ["LMHEAD_BWD_PERSISTENT"] = old
-    return a, b
+    _same_bits(out["1"], out["2"])
+    return out["0"], out["1"]
 
 
 def _blocks(x):
