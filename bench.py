@@ -32,7 +32,7 @@ METRIC = "tokens/s and TFLOP/s of fused logp+entropy fwd+bwd; % of GB300 BF16 te
 UNIT = "tokens/s"
 # GEMM kernels and their algorithmic flops per step in units of T_v*H*V
 GEMM_KERNELS = {"fwd_stats_gemm": 2.0, "bwd_dz_gemm": 2.0, "bwd_grad_gemm": 4.0,
-                "bwd_all_gemm": 6.0}
+                "bwd_all_gemm": 6.0, "bwd_window_gemm": 6.0}
 
 
 def parse():
