@@ -202,12 +202,25 @@ class OracleSample:
                 "rows), %.2f s per pass" % (n, self.w.name, self.w.V, dt))
 
 
+def cpu_model():
+    """Host CPU description (model name, or the architecture where /proc has none)."""
+    import platform
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip() + " (" + platform.machine() + ")"
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(name, seconds):
     s = OracleSample(name)
     n = s.calibrate(seconds)
     scored, dt = s.run(n)
     return {"value": scored / dt, "unit": UNIT, "cores": s.o.num_threads(), "kind": "oracle",
-            "sample": s.describe(n, dt)}
+            "sample": s.describe(n, dt), "affinity_cores": len(os.sched_getaffinity(0)),
+            "cpu": cpu_model()}
 
 
 def run_reference(args, rank, world):

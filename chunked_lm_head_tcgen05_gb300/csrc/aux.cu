@@ -3,6 +3,7 @@
 // log-sum-exp combine of per-split statistics, the per-row backward
 // coefficients and the zeroing of unscored rows.
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -15,7 +16,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kCompactThreads = 1024;
+constexpr int kCompactThreads = 256;
 
 // Wrap of negative ids (y in [-V, 0) -> y + V); -1 when the id is invalid.
 __device__ __forceinline__ int wrap_target(int y, int V) {
@@ -29,53 +30,107 @@ __global__ void clear_state_kernel(DeviceState* st, int rows) {
   st->abort_all = 0;
 }
 
-// One CTA: stable compaction of the scored positions (ascending order), the
-// wrapped targets in compact order, and the scored count.
+// Stable compaction of the scored positions, in two launches over chunks of
+// kCompactChunk tokens (one CTA each, kCompactThreads threads).  In a chunk,
+// thread t owns positions t, t + 256, ..., t + 15 * 256, so every load is
+// coalesced; within one round of 256 positions a warp ballot orders them.
+// (1) compact_count_kernel: scored tokens per chunk.
+// (2) compact_scatter_kernel: the chunk's offset (sum of the counts before
+//     it), the compact index and wrapped targets in ascending token order,
+//     the scored count, and -1 targets for the padding rows.
+constexpr int kCompactRounds = kCompactChunk / kCompactThreads;   // 16
+
+__device__ __forceinline__ int block_sum(int v, int* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int k = 0; k < kCompactThreads / 32; ++k) t += red[k];
+  return t;
+}
+
 __global__ void __launch_bounds__(kCompactThreads)
-    compact_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ targets, int T,
-                   int V, int T_alloc, int* __restrict__ idx, int* __restrict__ y_c,
-                   DeviceState* st) {
-  __shared__ int warp_tot[kCompactThreads / 32];
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, w = tid >> 5;
-  const int seg = (T + kCompactThreads - 1) / kCompactThreads;
-  const int b = min(T, tid * seg);
-  const int e = min(T, b + seg);
+    compact_count_kernel(const uint8_t* __restrict__ mask, int T, int* __restrict__ counts) {
+  __shared__ int red[kCompactThreads / 32];
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kCompactChunk;
   int cnt = 0;
-  for (int t = b; t < e; ++t) cnt += mask[t] != 0;
-  int incl = cnt;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += x;
+  for (int c = 0; c < kCompactRounds; ++c) {
+    const int64_t t = base + c * kCompactThreads + threadIdx.x;
+    if (t < T) cnt += mask[t] != 0;
   }
-  if (lane == 31) warp_tot[w] = incl;
+  const int tot = block_sum(cnt, red);
+  if (threadIdx.x == 0) counts[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(kCompactThreads)
+    compact_scatter_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ targets,
+                           int T, int V, int T_alloc, const int* __restrict__ counts, int n_chunks,
+                           int* __restrict__ idx, int* __restrict__ y_c, DeviceState* st) {
+  __shared__ int red[kCompactThreads / 32];
+  __shared__ int round_warp[kCompactRounds][kCompactThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // offset of this chunk and the total, from the per-chunk counts
+  int before = 0, all = 0;
+  for (int k = threadIdx.x; k < n_chunks; k += kCompactThreads) {
+    const int c = counts[k];
+    all += c;
+    if (k < static_cast<int>(blockIdx.x)) before += c;
+  }
+  before = block_sum(before, red);
+  all = block_sum(all, red);
+  // per round: a ballot orders this warp's 32 positions; warp totals in shared memory
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kCompactChunk;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t live = 0;          // bit c: position of round c is scored
+  int rank[kCompactRounds];   // rank among the scored positions of this warp's round
+#pragma unroll
+  for (int c = 0; c < kCompactRounds; ++c) {
+    const int64_t t = base + c * kCompactThreads + threadIdx.x;
+    const bool f = t < T && mask[t] != 0;
+    const uint32_t b = __ballot_sync(0xffffffffu, f);
+    rank[c] = __popc(b & lt);
+    if (f) live |= 1u << c;
+    if (lane == 0) round_warp[c][w] = __popc(b);
+  }
   __syncthreads();
+  // exclusive prefix over (round, warp) in position order: one warp scans 128 totals
   if (w == 0) {
-    int s = warp_tot[lane];
+    int carry = 0;
+    for (int c = 0; c < kCompactRounds; ++c) {
+      const int v = lane < kCompactThreads / 32 ? round_warp[c][lane] : 0;
+      int incl = v;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int x = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += x;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (lane < kCompactThreads / 32) round_warp[c][lane] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    warp_tot[lane] = s;   // inclusive prefix over warps
   }
   __syncthreads();
-  int pos = incl - cnt + (w > 0 ? warp_tot[w - 1] : 0);
-  const int total = warp_tot[kCompactThreads / 32 - 1];
   int bad = 0;
-  for (int t = b; t < e; ++t) {
-    if (mask[t]) {
+#pragma unroll
+  for (int c = 0; c < kCompactRounds; ++c) {
+    if (live & (1u << c)) {
+      const int t = static_cast<int>(base) + c * kCompactThreads + threadIdx.x;
+      const int pos = before + round_warp[c][w] + rank[c];
       const int y = wrap_target(targets[t], V);
-      bad |= (y < 0);
+      bad |= y < 0;
       idx[pos] = t;
       y_c[pos] = y;
-      ++pos;
     }
   }
-  for (int r = total + tid; r < T_alloc; r += kCompactThreads) y_c[r] = -1;
+  for (int r = all + static_cast<int>(blockIdx.x) * kCompactThreads + threadIdx.x; r < T_alloc;
+       r += n_chunks * kCompactThreads)
+    y_c[r] = -1;
   if (bad) atomicCAS(&st->status, 0, STATUS_BAD_TARGET);
-  if (tid == 0) st->rows = total;
+  if (blockIdx.x == 0 && threadIdx.x == 0) st->rows = all;
 }
 
 __global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T, int V, int T_alloc,
@@ -91,18 +146,19 @@ __global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T,
 }
 
 // h_c[r] = hidden[idx[r]] for scored rows; zero rows up to T_alloc so that
-// every tile edge past the scored count reads exact zeros.
+// every tile edge past the scored count reads exact zeros.  One row per CTA
+// iteration, 16-byte accesses.
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, int H8, const int* __restrict__ idx,
                                    int T_alloc, const DeviceState* st, uint4* __restrict__ h_c) {
   const int rows = st->rows;
-  const int64_t n = static_cast<int64_t>(T_alloc) * H8;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i / H8);
-    const int c = static_cast<int>(i - static_cast<int64_t>(r) * H8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < rows) v = hidden[static_cast<int64_t>(idx[r]) * H8 + c];
-    h_c[i] = v;
+  for (int r = blockIdx.x; r < T_alloc; r += gridDim.x) {
+    uint4* dst = h_c + static_cast<int64_t>(r) * H8;
+    if (r < rows) {
+      const uint4* src = hidden + static_cast<int64_t>(idx[r]) * H8;
+      for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = src[c];
+    } else {
+      for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = make_uint4(0, 0, 0, 0);
+    }
   }
 }
 
@@ -169,11 +225,10 @@ __global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* 
 
 __global__ void zero_masked_rows_kernel(const uint8_t* __restrict__ mask, int T, int H4,
                                         float4* __restrict__ d_hidden) {
-  const int64_t n = static_cast<int64_t>(T) * H4;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / H4);
-    if (!mask[t]) d_hidden[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (mask[t]) continue;
+    float4* row = d_hidden + static_cast<int64_t>(t) * H4;
+    for (int c = threadIdx.x; c < H4; c += blockDim.x) row[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -191,41 +246,52 @@ __global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* _
   // rows the gradient GEMMs read: whole 128-row tiles (zero padding rows included)
   const int rows = min(rows_cap, (dyn + BM - 1) / BM * BM);
   const int groups = (V + 7) / 8;
-  const int64_t n = static_cast<int64_t>(rows) * groups;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(i / groups);
-    const int c0 = static_cast<int>(i - static_cast<int64_t>(r) * groups) * 8;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const float4 cf = coef[t0 + r];
     const int y = y_c[t0 + r];
-    const float base = m_tile[static_cast<int64_t>(r) * mt_ld + c0 / BN] - cf.x;
-    uint16_t* row = z + static_cast<int64_t>(r) * ld + c0;
-    const uint4 raw = *reinterpret_cast<const uint4*>(row);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t out[4];
+    const float* mt = m_tile + static_cast<int64_t>(r) * mt_ld;
+    uint16_t* zr = z + static_cast<int64_t>(r) * ld;
+    for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
+      const int c0 = gi * 8;
+      const float base = mt[c0 / BN] - cf.x;
+      uint16_t* row = zr + c0;
+      const uint4 raw = *reinterpret_cast<const uint4*>(row);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t out[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-      float g[2];
-      const float uu[2] = {u.x, u.y};
+      for (int k = 0; k < 4; ++k) {
+        const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        float g[2];
+        const float uu[2] = {u.x, u.y};
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float d = uu[e] + base;
-        const float pr = exp2f(d);
-        g[e] = -pr * fmaf(cf.y, d, cf.z);
-        if (c0 + 2 * k + e == y) g[e] += cf.w;
+        for (int e = 0; e < 2; ++e) {
+          const float d = uu[e] + base;
+          const float pr = ex2_approx(d);
+          g[e] = -pr * fmaf(cf.y, d, cf.z);
+          if (c0 + 2 * k + e == y) g[e] += cf.w;
+        }
+        const __nv_bfloat162 b = __floats2bfloat162_rn(g[0], g[1]);
+        out[k] = *reinterpret_cast<const uint32_t*>(&b);
       }
-      const __nv_bfloat162 b = __floats2bfloat162_rn(g[0], g[1]);
-      out[k] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    if (c0 + 8 <= V) {
-      *reinterpret_cast<uint4*>(row) = make_uint4(out[0], out[1], out[2], out[3]);
-    } else {
+      if (c0 + 8 <= V) {
+        *reinterpret_cast<uint4*>(row) = make_uint4(out[0], out[1], out[2], out[3]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (c0 + j < V) row[j] = static_cast<uint16_t>((j & 1) ? (out[j >> 1] >> 16) : (out[j >> 1] & 0xFFFFu));
+        for (int j = 0; j < 8; ++j)
+          if (c0 + j < V)
+            row[j] = static_cast<uint16_t>((j & 1) ? (out[j >> 1] >> 16) : (out[j >> 1] & 0xFFFFu));
+      }
     }
   }
+}
+
+// Threads per CTA for a kernel that sweeps one row of `vecs` 16-byte
+// vectors per CTA iteration: the largest of 256, 128, 64, 32 that divides the
+// row, so that no pass over a row leaves warps idle.
+int row_threads(int vecs) {
+  for (int t = 256; t >= 32; t >>= 1)
+    if (vecs % t == 0) return t;
+  return 256;
 }
 
 int grid_for(int64_t n, int threads, int cap = 4 * 152 * 8) {
@@ -241,9 +307,17 @@ cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t 
   return cudaGetLastError();
 }
 
+int compact_chunks(int T) { return (T + kCompactChunk - 1) / kCompactChunk; }
+
 cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
-                           int* idx, int* y_c, DeviceState* st, cudaStream_t s) {
-  compact_kernel<<<1, kCompactThreads, 0, s>>>(mask, targets, T, V, T_alloc, idx, y_c, st);
+                           int* counts, int* idx, int* y_c, DeviceState* st, cudaStream_t s) {
+  const int n = compact_chunks(T);
+  if (n < 1) return cudaSuccess;
+  compact_count_kernel<<<n, kCompactThreads, 0, s>>>(mask, T, counts);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_scatter_kernel<<<n, kCompactThreads, 0, s>>>(mask, targets, T, V, T_alloc, counts, n, idx,
+                                                      y_c, st);
   return cudaGetLastError();
 }
 
@@ -256,7 +330,7 @@ cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_all
 cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
                                const DeviceState* st, uint16_t* h_c, cudaStream_t s) {
   const int H8 = H / 8;
-  gather_rows_kernel<<<grid_for(static_cast<int64_t>(T_alloc) * H8, 256), 256, 0, s>>>(
+  gather_rows_kernel<<<grid_for(T_alloc, 1, 152 * 32), row_threads(H8), 0, s>>>(
       reinterpret_cast<const uint4*>(hidden), H8, idx, T_alloc, st, reinterpret_cast<uint4*>(h_c));
   return cudaGetLastError();
 }
@@ -288,16 +362,15 @@ cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r
 cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_tile_ld,
                             const float4* coef, const int* y_c, const DeviceState* st, int t0,
                             int rows_cap, int V, cudaStream_t s) {
-  const int64_t n = static_cast<int64_t>(rows_cap) * ((V + 7) / 8);
-  fused_dz_kernel<<<grid_for(n, 256, 152 * 16), 256, 0, s>>>(z16, ld, m_tile, m_tile_ld, coef, y_c,
-                                                             st, t0, rows_cap, V);
+  fused_dz_kernel<<<grid_for(rows_cap, 1, 152 * 8), 256, 0, s>>>(z16, ld, m_tile, m_tile_ld, coef,
+                                                                 y_c, st, t0, rows_cap, V);
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
                                     cudaStream_t s) {
   const int H4 = H / 4;
-  zero_masked_rows_kernel<<<grid_for(static_cast<int64_t>(T) * H4, 256), 256, 0, s>>>(
+  zero_masked_rows_kernel<<<grid_for(T, 1, 152 * 32), row_threads(H4), 0, s>>>(
       mask, T, H4, reinterpret_cast<float4*>(d_hidden));
   return cudaGetLastError();
 }

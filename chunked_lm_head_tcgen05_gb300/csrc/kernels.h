@@ -154,8 +154,12 @@ cudaError_t launch_gemm_bwd_grad(const LaunchArgs& a, int grid, bool pair, cudaS
 cudaError_t launch_gemm_fwd_z(const LaunchArgs& a, int grid, bool pair, cudaStream_t s);
 
 // Auxiliary kernels (aux.cu).
+// Mask compaction works on chunks of this many tokens; `counts` holds one
+// int per chunk (compact_chunks(T) of them).
+constexpr int kCompactChunk = 4096;
+int compact_chunks(int T);
 cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
-                           int* idx, int* y_c, DeviceState* st, cudaStream_t s);
+                           int* counts, int* idx, int* y_c, DeviceState* st, cudaStream_t s);
 cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
                                  DeviceState* st, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,

@@ -280,7 +280,7 @@ FusedPlan plan_fused(int64_t T, int64_t H, int64_t V, int64_t chunk) {
 }
 
 struct Layout {
-  size_t state, counters, idx, y_c, h_c, part, coef, dz, m_tile, total;
+  size_t state, counters, chunk_counts, idx, y_c, h_c, part, coef, dz, m_tile, total;
   int64_t n_counters;   // dynamic work-unit counters, one per GEMM launch
 };
 
@@ -307,6 +307,7 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
     L.n_counters = 2 * plan_fused(T, H, V, chunk).n_tb;
   }
   L.counters = take(4 * static_cast<size_t>(L.n_counters));
+  L.chunk_counts = take(4 * static_cast<size_t>(compact_chunks(static_cast<int>(T_alloc))));
   L.idx = take(4 * static_cast<size_t>(T_alloc));
   L.y_c = take(4 * static_cast<size_t>(T_alloc));
   L.h_c = take(2 * static_cast<size_t>(T_alloc) * static_cast<size_t>(H));
@@ -367,7 +368,8 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
     f->idx = reinterpret_cast<int*>(ws + L.idx);
     uint16_t* h_c = reinterpret_cast<uint16_t*>(ws + L.h_c);
     LMH_TRY(launch("compact", s, [&] {
-      return launch_compact(mask, targets, Ti, V, Ta, f->idx, f->y_c, f->st, s);
+      return launch_compact(mask, targets, Ti, V, Ta, reinterpret_cast<int*>(ws + L.chunk_counts),
+                            f->idx, f->y_c, f->st, s);
     }));
     LMH_TRY(launch("gather_rows", s, [&] {
       return launch_gather_rows(hidden, H, f->idx, Ta, f->st, h_c, s);
