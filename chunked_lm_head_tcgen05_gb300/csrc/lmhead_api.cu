@@ -73,13 +73,15 @@ cudaError_t launch(const char* name, cudaStream_t s, F&& f) {
 
 // ------------------------------------------------------------------ device facts
 int sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];   // per device; 0 = not yet known
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    if (const int c = cache[dev].load(std::memory_order_relaxed); c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

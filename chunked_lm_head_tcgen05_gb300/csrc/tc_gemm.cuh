@@ -40,6 +40,7 @@
 #include "kernels.h"
 #include "ptx.cuh"
 
+#include <atomic>
 #include <climits>
 
 namespace lmh {
@@ -779,10 +780,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // Co-resident clusters of two for a kernel (cached per kernel and device).
 template <class K>
 int max_active_pairs(K kern) {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];   // per device; 0 = not yet known
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev] > 0) return cache[dev];
+  if (const int c = cache[dev].load(std::memory_order_relaxed); c > 0) return c;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
@@ -796,7 +797,7 @@ int max_active_pairs(K kern) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
-  cache[dev] = n;
+  cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
