@@ -646,39 +646,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-int bwd_all_max_pairs() {
-  static std::atomic<int> cache[64];   // per device; 0 = not yet known
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (const int c = cache[dev].load(std::memory_order_relaxed); c > 0) return c;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = BWD_ALL_SMEM_BYTES;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, bwd_all_kernel, &cfg) != cudaSuccess) return 0;
-  cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_gemm_bwd_all(const BwdAllArgs& a, int grid, cudaStream_t s) {
   if (a.n_tb < 1 || a.n_tb > BWD_ALL_MAX_TOKEN_BLOCKS || a.n_vb < 1 || a.T_b % (2 * BM) != 0 ||
       a.V_b % BN != 0 || a.H % BK != 0)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_all_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(BWD_ALL_SMEM_BYTES));
+  static std::atomic<int> ready[64];   // per device
+  int pairs_max = 0;
+  const cudaError_t e = prepare_kernel(ready, reinterpret_cast<const void*>(bwd_all_kernel),
+                                       BWD_ALL_SMEM_BYTES, true, &pairs_max);
   if (e != cudaSuccess) return e;
-  const int pairs_max = bwd_all_max_pairs();
-  if (pairs_max <= 0) return cudaErrorInvalidConfiguration;
   int pairs = (grid + 1) / 2;
   if (pairs < 1) pairs = 1;
   if (pairs > pairs_max) pairs = pairs_max;

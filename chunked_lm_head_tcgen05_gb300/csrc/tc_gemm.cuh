@@ -777,17 +777,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
 }
 
-// Co-resident clusters of two for a kernel (cached per kernel and device).
-template <class K>
-int max_active_pairs(K kern) {
-  static std::atomic<int> cache[64];   // per device; 0 = not yet known
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (const int c = cache[dev].load(std::memory_order_relaxed); c > 0) return c;
+// Co-resident clusters of two CTAs of `kern` with `smem` bytes of dynamic
+// shared memory each (0 if the query fails).
+inline int cluster_pairs(const void* kern, size_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -797,8 +793,31 @@ int max_active_pairs(K kern) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
-  cache[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+// Once per kernel and device: allow its dynamic shared memory and count its
+// co-resident pairs.  `ready` holds 0 (not yet done) or 1 + that count, so
+// later launches make no configuration calls (which also keeps them legal
+// inside a stream capture).
+inline cudaError_t prepare_kernel(std::atomic<int>* ready, const void* kern, size_t smem,
+                                  bool pair, int* pairs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int r = ready[dev].load(std::memory_order_relaxed);
+  if (r == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int n = pair ? cluster_pairs(kern, smem) : 0;
+    if (pair && n <= 0) return cudaErrorInvalidConfiguration;
+    r = 1 + n;
+    ready[dev].store(r, std::memory_order_relaxed);
+  }
+  *pairs = r - 1;
+  return cudaSuccess;
 }
 
 // grid = CTAs wanted (ignored beyond the co-resident limit).  For pairs the
@@ -806,13 +825,13 @@ int max_active_pairs(K kern) {
 template <int EPI, bool B_MN, bool PAIR>
 cudaError_t launch_tc_gemm(const LaunchArgs& a, int grid, cudaStream_t s) {
   auto kern = tc_gemm_kernel<EPI, B_MN, PAIR>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(GEMM_SMEM_BYTES));
+  static std::atomic<int> ready[64];   // per device, for this kernel
+  int pairs_max = 0;
+  const cudaError_t e = prepare_kernel(ready, reinterpret_cast<const void*>(kern),
+                                       GEMM_SMEM_BYTES, PAIR, &pairs_max);
   if (e != cudaSuccess) return e;
   int ctas = grid < 1 ? 1 : grid;
   if constexpr (PAIR) {
-    const int pairs_max = max_active_pairs(kern);
-    if (pairs_max <= 0) return cudaErrorInvalidConfiguration;
     int pairs = (ctas + 1) / 2;
     if (pairs > pairs_max) pairs = pairs_max;
     ctas = 2 * pairs;
