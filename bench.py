@@ -273,12 +273,13 @@ def run_ours(args, rank, world, local):
                          lm.lmhead_workspace_size(1, T, H, V, c)), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(src):
+    def step(src, on=None):
+        st = stream if on is None else on
         rc = lm.lmhead_logps_fwd(src["hidden"], g["weight"], src["targets"], src["loss_mask"], tau,
-                                 c, logp, ent, lse, ws, stream)
+                                 c, logp, ent, lse, ws, st)
         rc |= lm.lmhead_logps_bwd(src["hidden"], g["weight"], src["targets"], src["loss_mask"],
                                   tau, c, src["grad_logp"], src["grad_entropy"], lse, ent, dh, dw,
-                                  0, ws, stream)
+                                  0, ws, st)
         if rc:
             raise lm.LmheadError(rc, "step")
 
@@ -423,6 +424,27 @@ def run_ours(args, rank, world, local):
         "plan": {"fwd_splits": splits, "bwd_tokens": tb_rows, "bwd_vocab": vb_cols},
     }
 
+    # ---- the same step captured once in a CUDA graph and replayed (launch overhead removed)
+    graph_replay = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(g, side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step(g, torch.cuda.current_stream(dev))   # the capturing stream
+        cg.replay()
+        torch.cuda.synchronize()
+        tg = max_over_ranks(timed(cg.replay, nb), world) / nb
+        graph_replay = {"value": Tv * world / tg, "unit": UNIT, "ms_per_step": tg * 1e3}
+        del cg
+    except Exception as exc:   # report, do not fail the bench
+        graph_replay = {"error": str(exc)[:200]}
+    stream = torch.cuda.current_stream(dev)
+
     # ---- device memory: the library allocates nothing; its workspace is bounded by the chunk
     torch.cuda.synchronize()
     base = torch.cuda.memory_allocated(dev)
@@ -456,6 +478,7 @@ def run_ours(args, rank, world, local):
         "roofline": roofline,
         "kernels": kernels,
         "breakdown": breakdown,
+        "graph_replay": graph_replay,
         "memory": memory,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
