@@ -37,7 +37,7 @@ NOALLOC_SCRATCH_BYTES = 64 << 20   # LMHEAD_NOALLOC_SCRATCH_BYTES in include/lmh
 STATUS_NAMES = {
     0: "LMHEAD_OK", 1: "LMHEAD_ERR_INVALID_ARG", 2: "LMHEAD_ERR_UNSUPPORTED",
     3: "LMHEAD_ERR_WORKSPACE_TOO_SMALL", 4: "LMHEAD_ERR_CUDA",
-    5: "LMHEAD_ERR_DEVICE_TIMEOUT", 6: "LMHEAD_ERR_BAD_TARGET",
+    5: "LMHEAD_ERR_DEVICE_TIMEOUT", 6: "LMHEAD_ERR_BAD_TARGET", 7: "LMHEAD_ERR_INTERNAL",
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
           }
           stage_out(pk, stg0, nstore++, lrow, issuer, &A.dz_k, 1, col0 + cc * 64,
-                    x.m * PAIR_M + r128);
+                    x.m * PAIR_M + r128, &st->status);
         }
         signal(F.dz_col(x.b, x.n), F.dz_all(x.b), true);
       } else if (x.kind == U_DH) {
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
             stage_out(w, stg0, nstore++, lrow, issuer, &A.dh_out, add ? 2 : 1, col0 + cb,
-                      x.k.t0 + x.m * PAIR_M + r128);
+                      x.k.t0 + x.m * PAIR_M + r128, &st->status);
           } else if (row_ok) {
             const int lim = A.H - col0 - cb;
             float* dst = A.d_hidden + orow * A.H + col0 + cb;
@@ -627,7 +627,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
           stage_out(w, stg0, nstore++, lrow, issuer, &A.dw_out, mode, col0 + c * 32,
-                    x.k.v0 + x.m * PAIR_M + r128);
+                    x.k.v0 + x.m * PAIR_M + r128, &st->status);
         }
         signal(F.dw_col(x.b, x.m), nullptr, true);
       }

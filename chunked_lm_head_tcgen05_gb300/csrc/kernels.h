@@ -30,6 +30,7 @@ constexpr size_t BWD_ALL_SMEM_BYTES = GEMM_SMEM_BYTES + 1024;   // + the token-b
 // Device status word values (same numbers as the public lmhead_status).
 constexpr int STATUS_DEVICE_TIMEOUT = 5;
 constexpr int STATUS_BAD_TARGET = 6;
+constexpr int STATUS_INTERNAL = 7;
 
 // Small block of device state at the head of the workspace.
 struct DeviceState {

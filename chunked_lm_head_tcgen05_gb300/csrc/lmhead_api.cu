@@ -413,6 +413,8 @@ const char* lmhead_status_string(lmhead_status status) {
     case LMHEAD_ERR_CUDA: return "LMHEAD_ERR_CUDA: CUDA launch or runtime error";
     case LMHEAD_ERR_DEVICE_TIMEOUT: return "LMHEAD_ERR_DEVICE_TIMEOUT: a device wait exceeded its limit";
     case LMHEAD_ERR_BAD_TARGET: return "LMHEAD_ERR_BAD_TARGET: a scored target lies outside [-V, V)";
+    case LMHEAD_ERR_INTERNAL:
+      return "LMHEAD_ERR_INTERNAL: a kernel refused a tile store at an invalid coordinate";
   }
   return "unknown lmhead_status";
 }

@@ -163,10 +163,13 @@ __device__ __forceinline__ int split_unit(const Sched& s0, int u, int& q) {
 // Write one thread's 128-byte row piece (8 x 16 bytes) into staging buffer
 // (nstore & 1) in the 128-byte swizzled layout and hand the 128-row tile to
 // TMA (store, or reduce-add for mode 2).  All 128 epilogue threads call it
-// together; `issuer` is the one thread that drives TMA.
+// together; `issuer` is the one thread that drives TMA.  Every tile store
+// starts at a non-negative row and at a column that is a multiple of 32
+// elements; a coordinate outside that is never issued (a TMA store there
+// would fault the context): it is recorded as STATUS_INTERNAL instead.
 __device__ __forceinline__ void stage_out(const uint32_t* w, uint32_t stg0, uint32_t nstore,
                                           int lrow, bool issuer, const CUtensorMap* map, int mode,
-                                          int x, int y) {
+                                          int x, int y, int* status) {
   const uint32_t buf = stg0 + (nstore & 1u) * 16384u;
   if (issuer && nstore >= 2) bulk_wait_read<1>();
   named_bar_sync(1, 128);
@@ -178,7 +181,9 @@ __device__ __forceinline__ void stage_out(const uint32_t* w, uint32_t stg0, uint
   fence_async_smem();
   named_bar_sync(1, 128);
   if (issuer) {
-    if (mode == 2)
+    if (x < 0 || y < 0 || (x & 31) != 0)
+      atomicCAS(status, 0, STATUS_INTERNAL);
+    else if (mode == 2)
       tma_reduce_add_2d(map, buf, x, y);
     else
       tma_store_2d(map, buf, x, y);
@@ -667,7 +672,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_f16x2(d[2 * k], d[2 * k + 1]);
             }
-            stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t);
+            stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t, status);
           }
           if (row < p.m_cap) p.m_tile[static_cast<int64_t>(row) * p.m_tile_ld + n] = mref;
         } else if constexpr (EPI == EPI_BWD_DZ) {
@@ -697,7 +702,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
             }
             if (p.out_mode == 1) {
-              stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t);
+              stage_out(pk, stg0, nstore++, lrow, issuer, map_out, 1, col0 + cc * 64, row_t, status);
             } else if (row_ok) {
               const int lim = p.n_extent - col0 - cc * 64;
               uint16_t* dst = p.dz_out + static_cast<int64_t>(row) * p.dz_ld + col0 + cc * 64;
@@ -726,7 +731,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               uint32_t w[32];
 #pragma unroll
               for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
-              stage_out(w, stg0, nstore++, lrow, issuer, map_out, p.out_mode, col0 + cb, row_t);
+              stage_out(w, stg0, nstore++, lrow, issuer, map_out, p.out_mode, col0 + cb, row_t,
+                        status);
             } else if (row_ok) {
               const int lim = p.n_extent - col0 - cb;
               float* dst = p.out + orow * p.out_ld + col0 + cb;

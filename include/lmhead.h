@@ -73,7 +73,9 @@ typedef enum {
   LMHEAD_ERR_WORKSPACE_TOO_SMALL = 3,
   LMHEAD_ERR_CUDA = 4,
   LMHEAD_ERR_DEVICE_TIMEOUT = 5, /* a device-side wait exceeded its limit */
-  LMHEAD_ERR_BAD_TARGET = 6      /* a scored target outside [-V, V) */
+  LMHEAD_ERR_BAD_TARGET = 6,     /* a scored target outside [-V, V) */
+  LMHEAD_ERR_INTERNAL = 7        /* a kernel refused a tile store at an invalid coordinate
+                                    instead of issuing it (a defect of this library) */
 } lmhead_status;
 
 enum { LMHEAD_OP_FWD = 0, LMHEAD_OP_BWD = 1, LMHEAD_OP_FWD_BWD = 2 };
@@ -246,8 +248,9 @@ lmhead_status lmhead_selftest_bounded_wait(void* workspace, size_t workspace_byt
 
 /*
  * Synchronises `stream`, then returns the device status word that the last
- * call using `workspace` left (LMHEAD_OK, LMHEAD_ERR_BAD_TARGET or
- * LMHEAD_ERR_DEVICE_TIMEOUT), or LMHEAD_ERR_CUDA if the read failed.
+ * call using `workspace` left (LMHEAD_OK, LMHEAD_ERR_BAD_TARGET,
+ * LMHEAD_ERR_DEVICE_TIMEOUT or LMHEAD_ERR_INTERNAL), or LMHEAD_ERR_CUDA if the
+ * read failed.
  */
 lmhead_status lmhead_read_device_status(const void* workspace, lmhead_stream_t stream);
 
