@@ -9,6 +9,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <utility>
 
 namespace lmh {
 
@@ -24,10 +25,19 @@ __device__ __forceinline__ int wrap_target(int y, int V) {
   return (y >= 0 && y < V) ? y : -1;
 }
 
-__global__ void clear_state_kernel(DeviceState* st, int rows) {
-  st->status = 0;
-  st->rows = rows;
-  st->abort_all = 0;
+// Start of every call: status, scored count (known on the host only when no
+// mask is given) and abort word, and the zeroed work-unit counters.
+__global__ void clear_state_kernel(DeviceState* st, int rows, int* counters, int64_t n) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    st->status = 0;
+    st->rows = rows;
+    st->abort_all = 0;
+  }
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    counters[i] = 0;
 }
 
 // Stable compaction of the scored positions, in two launches over chunks of
@@ -55,6 +65,8 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
 
 __global__ void __launch_bounds__(kCompactThreads)
     compact_count_kernel(const uint8_t* __restrict__ mask, int T, int* __restrict__ counts) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   __shared__ int red[kCompactThreads / 32];
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kCompactChunk;
   int cnt = 0;
@@ -71,6 +83,8 @@ __global__ void __launch_bounds__(kCompactThreads)
     compact_scatter_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ targets,
                            int T, int V, int T_alloc, const int* __restrict__ counts, int n_chunks,
                            int* __restrict__ idx, int* __restrict__ y_c, DeviceState* st) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   __shared__ int red[kCompactThreads / 32];
   __shared__ int round_warp[kCompactRounds][kCompactThreads / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -135,6 +149,8 @@ __global__ void __launch_bounds__(kCompactThreads)
 
 __global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T, int V, int T_alloc,
                                      int* __restrict__ y_c, DeviceState* st) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= T_alloc) return;
   int y = -1;
@@ -150,6 +166,8 @@ __global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T,
 // iteration, 16-byte accesses.
 __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, int H8, const int* __restrict__ idx,
                                    int T_alloc, const DeviceState* st, uint4* __restrict__ h_c) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   const int rows = st->rows;
   for (int r = blockIdx.x; r < T_alloc; r += gridDim.x) {
     uint4* dst = h_c + static_cast<int64_t>(r) * H8;
@@ -164,6 +182,8 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, int H8, con
 
 __global__ void zero_masked_outputs_kernel(const uint8_t* __restrict__ mask, int T, float* logp,
                                            float* entropy, float* lse) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T || mask[t]) return;
   logp[t] = 0.f;
@@ -179,6 +199,8 @@ __global__ void fwd_merge_kernel(const float4* __restrict__ part, int n_splits, 
                                  const int* __restrict__ idx, const int* __restrict__ y_c,
                                  const DeviceState* st, int r0, int r1, float* logp,
                                  float* entropy, float* lse) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   const int r = r0 + blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= r1 || r >= st->rows) return;
   float M = -INFINITY;
@@ -207,6 +229,8 @@ __global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* 
                                 const float* __restrict__ grad_logp,
                                 const float* __restrict__ grad_entropy, float inv_tau,
                                 float4* __restrict__ coef) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   const int r = r0 + blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= r1) return;
   float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -225,6 +249,8 @@ __global__ void bwd_prep_kernel(const int* __restrict__ idx, const DeviceState* 
 
 __global__ void zero_masked_rows_kernel(const uint8_t* __restrict__ mask, int T, int H4,
                                         float4* __restrict__ d_hidden) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     if (mask[t]) continue;
     float4* row = d_hidden + static_cast<int64_t>(t) * H4;
@@ -241,6 +267,8 @@ __global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* _
                                 int mt_ld, const float4* __restrict__ coef,
                                 const int* __restrict__ y_c, const DeviceState* st, int t0,
                                 int rows_cap, int V) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
   int dyn = st->rows - t0;
   dyn = dyn < 0 ? 0 : (dyn > rows_cap ? rows_cap : dyn);
   // rows the gradient GEMMs read: whole 128-row tiles (zero padding rows included)
@@ -285,6 +313,25 @@ __global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* _
   }
 }
 
+// Launch with programmatic dependent launch: the kernel may start while its
+// predecessor in the stream finishes; every helper kernel waits for the
+// predecessor's completion (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid < 1 ? 1 : grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Threads per CTA for a kernel that sweeps one row of `vecs` 16-byte
 // vectors per CTA iteration: the largest of 256, 128, 64, 32 that divides the
 // row, so that no pass over a row leaves warps idle.
@@ -302,9 +349,10 @@ int grid_for(int64_t n, int threads, int cap = 4 * 152 * 8) {
 
 }  // namespace
 
-cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s) {
-  clear_state_kernel<<<1, 1, 0, s>>>(st, rows_if_dense);
-  return cudaGetLastError();
+cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, int* counters,
+                               int64_t n_counters, cudaStream_t s) {
+  return launch_pdl(clear_state_kernel, grid_for(n_counters, 256, 152), 256, s, st,
+                    rows_if_dense, counters, n_counters);
 }
 
 int compact_chunks(int T) { return (T + kCompactChunk - 1) / kCompactChunk; }
@@ -313,66 +361,60 @@ cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, i
                            int* counts, int* idx, int* y_c, DeviceState* st, cudaStream_t s) {
   const int n = compact_chunks(T);
   if (n < 1) return cudaSuccess;
-  compact_count_kernel<<<n, kCompactThreads, 0, s>>>(mask, T, counts);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(compact_count_kernel, n, kCompactThreads, s, mask, T, counts);
   if (e != cudaSuccess) return e;
-  compact_scatter_kernel<<<n, kCompactThreads, 0, s>>>(mask, targets, T, V, T_alloc, counts, n, idx,
-                                                      y_c, st);
-  return cudaGetLastError();
+  return launch_pdl(compact_scatter_kernel, n, kCompactThreads, s, mask, targets, T, V, T_alloc,
+                    static_cast<const int*>(counts), n, idx, y_c, st);
 }
 
 cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
                                  DeviceState* st, cudaStream_t s) {
-  targets_dense_kernel<<<(T_alloc + 255) / 256, 256, 0, s>>>(targets, T, V, T_alloc, y_c, st);
-  return cudaGetLastError();
+  return launch_pdl(targets_dense_kernel, (T_alloc + 255) / 256, 256, s, targets, T, V, T_alloc,
+                    y_c, st);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
                                const DeviceState* st, uint16_t* h_c, cudaStream_t s) {
   const int H8 = H / 8;
-  gather_rows_kernel<<<grid_for(T_alloc, 1, 152 * 32), row_threads(H8), 0, s>>>(
-      reinterpret_cast<const uint4*>(hidden), H8, idx, T_alloc, st, reinterpret_cast<uint4*>(h_c));
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, grid_for(T_alloc, 1, 152 * 32), row_threads(H8), s,
+                    reinterpret_cast<const uint4*>(hidden), H8, idx, T_alloc, st,
+                    reinterpret_cast<uint4*>(h_c));
 }
 
 cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
                                        float* lse, cudaStream_t s) {
-  zero_masked_outputs_kernel<<<(T + 255) / 256, 256, 0, s>>>(mask, T, logp, entropy, lse);
-  return cudaGetLastError();
+  return launch_pdl(zero_masked_outputs_kernel, (T + 255) / 256, 256, s, mask, T, logp, entropy,
+                    lse);
 }
 
 cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
                              const int* y_c, const DeviceState* st, int r0, int r1, float* logp,
                              float* entropy, float* lse, cudaStream_t s) {
   if (r1 <= r0) return cudaSuccess;
-  fwd_merge_kernel<<<(r1 - r0 + 255) / 256, 256, 0, s>>>(partials, n_splits, part_ld, idx, y_c,
-                                                          st, r0, r1, logp, entropy, lse);
-  return cudaGetLastError();
+  return launch_pdl(fwd_merge_kernel, (r1 - r0 + 255) / 256, 256, s, partials, n_splits, part_ld,
+                    idx, y_c, st, r0, r1, logp, entropy, lse);
 }
 
 cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r1, const float* lse,
                             const float* entropy, const float* grad_logp,
                             const float* grad_entropy, float tau, float4* coef, cudaStream_t s) {
   if (r1 <= r0) return cudaSuccess;
-  bwd_prep_kernel<<<(r1 - r0 + 255) / 256, 256, 0, s>>>(idx, st, r0, r1, lse, entropy, grad_logp,
-                                                         grad_entropy, 1.0f / tau, coef);
-  return cudaGetLastError();
+  return launch_pdl(bwd_prep_kernel, (r1 - r0 + 255) / 256, 256, s, idx, st, r0, r1, lse, entropy,
+                    grad_logp, grad_entropy, 1.0f / tau, coef);
 }
 
 cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_tile_ld,
                             const float4* coef, const int* y_c, const DeviceState* st, int t0,
                             int rows_cap, int V, cudaStream_t s) {
-  fused_dz_kernel<<<grid_for(rows_cap, 1, 152 * 8), 256, 0, s>>>(z16, ld, m_tile, m_tile_ld, coef,
-                                                                 y_c, st, t0, rows_cap, V);
-  return cudaGetLastError();
+  return launch_pdl(fused_dz_kernel, grid_for(rows_cap, 1, 152 * 8), 256, s, z16, ld, m_tile,
+                    m_tile_ld, coef, y_c, st, t0, rows_cap, V);
 }
 
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
                                     cudaStream_t s) {
   const int H4 = H / 4;
-  zero_masked_rows_kernel<<<grid_for(T, 1, 152 * 32), row_threads(H4), 0, s>>>(
-      mask, T, H4, reinterpret_cast<float4*>(d_hidden));
-  return cudaGetLastError();
+  return launch_pdl(zero_masked_rows_kernel, grid_for(T, 1, 152 * 32), row_threads(H4), s, mask, T,
+                    H4, reinterpret_cast<float4*>(d_hidden));
 }
 
 }  // namespace lmh

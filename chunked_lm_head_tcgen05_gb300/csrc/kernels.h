@@ -183,7 +183,10 @@ cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_ti
                             int rows_cap, int V, cudaStream_t s);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
                                     cudaStream_t s);
-cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, cudaStream_t s);
+// Resets the device state (status, scored count, abort word) and zeroes
+// `n_counters` work-unit counters.
+cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, int* counters,
+                               int64_t n_counters, cudaStream_t s);
 
 // Self-test of the bounded mbarrier wait (selftest.cu).
 cudaError_t launch_bounded_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t s);

@@ -363,9 +363,9 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
   f->y_c = reinterpret_cast<int*>(ws + L.y_c);
   const int Ti = static_cast<int>(T), Ta = static_cast<int>(f->T_alloc);
   f->counters = reinterpret_cast<int*>(ws + L.counters);
-  if (cudaMemsetAsync(f->counters, 0, 4 * static_cast<size_t>(L.n_counters), s) != cudaSuccess)
-    return LMHEAD_ERR_CUDA;
-  LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(f->st, mask ? 0 : Ti, s); }));
+  LMH_TRY(launch("clear_state", s, [&] {
+    return launch_clear_state(f->st, mask ? 0 : Ti, f->counters, L.n_counters, s);
+  }));
   if (mask) {
     f->idx = reinterpret_cast<int*>(ws + L.idx);
     uint16_t* h_c = reinterpret_cast<uint16_t*>(ws + L.h_c);
@@ -911,7 +911,7 @@ lmhead_status lmhead_selftest_bounded_wait(void* workspace, size_t workspace_byt
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return LMHEAD_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   DeviceState* st = static_cast<DeviceState*>(workspace);
-  LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(st, 0, s); }));
+  LMH_TRY(launch("clear_state", s, [&] { return launch_clear_state(st, 0, nullptr, 0, s); }));
   LMH_TRY(launch("bounded_wait_selftest", s, [&] {
     return launch_bounded_wait_selftest(&st->status, uint64_t{limit_ms} * 1000000ull, s);
   }));
