@@ -10,6 +10,11 @@ import oracle
 
 # logp / entropy: absolute; lse: absolute; gradients: relative Frobenius
 LIMITS = {"logp": 2e-3, "entropy": 2e-3, "lse": 1e-3, "d_hidden": 1e-2, "d_weight": 1e-2}
+# A gradient whose exact value is identically zero (a one-entry vocabulary:
+# p = 1, so dz = 0) has no relative error; there the largest |value| is held
+# to this absolute bound.  The kernels leave fp32 rounding residue there: p is
+# 2^d with d = z log2(e) - lse log2(e) rounded in fp32, |d| ~ 1e-7.
+ZERO_REF_ATOL = 1e-4
 
 _built = False
 
@@ -98,7 +103,7 @@ def errors(gpu, ora, rows=None, keys=("logp", "entropy", "lse", "d_hidden", "d_w
         a = gpu[k] if rows is None or k == "d_weight" else gpu[k][rows]
         b = ora[k]
         if k in ("d_hidden", "d_weight"):
-            e[k] = rel_fro(a, b)
+            e[k] = rel_fro(a, b) if np.any(b != 0) else (float(np.abs(a).max()) if a.size else 0.0)
         else:
             fin = np.isfinite(b)
             assert np.array_equal(np.isfinite(a), fin), "non-finite pattern differs for %s" % k
@@ -108,7 +113,10 @@ def errors(gpu, ora, rows=None, keys=("logp", "entropy", "lse", "d_hidden", "d_w
 
 def assert_parity(gpu, ora, rows=None, keys=("logp", "entropy", "lse", "d_hidden", "d_weight")):
     e = errors(gpu, ora, rows, keys)
-    bad = {k: v for k, v in e.items() if not v <= LIMITS[k]}
+    zero_ref = {k for k in ("d_hidden", "d_weight")
+                if k in e and not np.any(np.asarray(ora[k]) != 0)}
+    bad = {k: v for k, v in e.items()
+           if not v <= (ZERO_REF_ATOL if k in zero_ref else LIMITS[k])}
     assert not bad, "parity failed: %s (all: %s)" % (bad, e)
     return e
 
