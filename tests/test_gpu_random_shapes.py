@@ -1,8 +1,10 @@
 """Seeded random configurations against the oracle: token counts, hidden and
 vocabulary sizes, chunk sizes, temperatures, mask styles, missing
 cotangents and d_weight accumulation drawn together, at sizes the oracle
-finishes in about a second each.  Every fourth case also runs the opt-in
-single-kernel backward forms and requires the same bits as the default."""
+finishes in about a second each.  Each case also runs the single-call path
+with kept logits (the fp16 logit store and in-place cotangent pass) against
+the oracle, and every fourth case the opt-in single-kernel backward forms,
+which must give the default path's bits."""
 import os
 
 import numpy as np
@@ -12,7 +14,7 @@ import torch
 import chunked_lm_head_tcgen05_gb300 as lm
 from chunked_lm_head_tcgen05_gb300 import workloads as W
 
-from gpu_helpers import assert_parity, run_gpu, run_oracle
+from gpu_helpers import assert_parity, run_gpu, run_gpu_fwd_bwd, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +56,10 @@ def test_random_configuration(i):
     if init is not None:
         o["d_weight"] = o["d_weight"] + init.double().numpy()
     e = assert_parity(g, o)
+    k = run_gpu_fwd_bwd(x, lm.LMHEAD_STRATEGY_KEEP_LOGITS, grad_entropy=opts["grad_entropy"],
+                        accumulate=opts["accumulate"], d_weight_init=init)
+    assert k["status"] == 0
+    ek = assert_parity(k, o)
     if i % 4 == 0:
         old = os.environ.get("LMHEAD_BWD_PERSISTENT")
         try:
@@ -69,4 +75,4 @@ def test_random_configuration(i):
             else:
                 os.environ["LMHEAD_BWD_PERSISTENT"] = old
     print(i, dict(T=w.T, H=w.H, V=w.V, chunk=w.chunk_size, tau=w.temperature, mask=w.mask),
-          opts, e)
+          opts, e, ek)
