@@ -17,18 +17,17 @@
  *   d_hidden_t  = sum_v (dz_v / tau) W_v
  *   d_weight_v += sum_t (dz_v / tau) h_t
  *
- * Sources: the chunked LM head ("Compute cross-entropy loss in chunks
- * instead of materializing the full logits tensor", SkyRL issue #891
- * "[tx] support long sequence", section "What Each Optimization Does", item
- * 4); the fused log-prob head (tunix PR #2913, commit "fused sharded
- * log-prob head (TUNIX_LOGPS_SHARDED_HEAD=fused)" and section "How the fused
- * log-prob head works": one pass over a chunk's logits gives the target
- * logit by a one-hot select, the max and exp-sum, and the entropy from the
- * same exponentials; the max and exp-sum are kept for the backward; the
- * backward forms the logits' cotangent in one elementwise pass over
- * recomputed logits and both gradient matmuls read that one cotangent);
- * log-sum-exp merging of partial results ("Long Sequences (SeCO)",
- * section "Efficiency").
+ * Sources (cited by page and section): SkyRL issue #891 "[tx] support long
+ * sequence", section "What Each Optimization Does", item 4 -- the loss is
+ * computed chunk by chunk so the [T, V] logits never exist at once; tunix
+ * PR #2913, section "How the fused log-prob head works" -- a single pass
+ * over a chunk's logits yields the target logit (one-hot selection), the
+ * row maximum and exponential sum, and the entropy from those same
+ * exponentials, the maximum and sum being saved for the backward, which
+ * recomputes the logits, turns them into their cotangent elementwise, and
+ * feeds that single cotangent to both gradient products; the palingenesis guide
+ * "Long Sequences (SeCO)", section "Efficiency" -- partial results are
+ * combined by their log-sum-exp.
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The

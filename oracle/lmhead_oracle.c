@@ -27,7 +27,8 @@
  *    (TUNIX_LOGPS_SHARDED_HEAD=fused)": a chunk's logits give the target
  *    logit (one-hot select), the max and exp-sum, and the entropy from the
  *    same exponentials; section "How the fused log-prob head works": a
- *    token's log-prob is target - (log exp-sum + max); the temperature
+ *    log-probability equals the target logit minus (max + log of the shifted
+ *    exponential sum); the temperature
  *    divides the logits (tested at 0.7 and 1) and the backward keeps that
  *    division; negative ids wrap and ids are valid in [0, vocab) (review
  *    thread on _target_hit).
@@ -251,8 +252,8 @@ int lmo_backward(int64_t T, int32_t H, int32_t V,
 
 /*
  * Logits-level scoring (for callers that already hold a chunk's logits).
- * The pages test their fused scoring on logits with inf, -inf and NaN
- * entries and a row of no finite logit, and list the isfinite mask of the
+ * The pages test their fused scoring on logits containing infinities and
+ * NaNs, including a row without any finite entry, and list the isfinite mask of the
  * cotangent among the parts a test must catch (tunix PR #2913, commit
  * "fused sharded log-prob head": FusedScoringTest), but print no values.
  * This file reads them as follows, with z = logits / tau per row:
