@@ -46,11 +46,18 @@
  *  - T == 0 is a no-op that returns LMHEAD_OK (the backward still zeroes
  *    d_weight unless accumulate_dweight is set).
  *  - Conditions found on the device (an unmasked target outside [-V, V), a
- *    bounded wait that gave up) are recorded in a status word inside the
- *    workspace; lmhead_read_device_status() returns it.
+ *    bounded wait that gave up, a tile store refused at an invalid
+ *    coordinate) are recorded in a status word inside the workspace;
+ *    lmhead_read_device_status() returns it.
  *  - Calls are reentrant as long as concurrent calls use distinct
  *    workspaces.  Results are deterministic: the same inputs, shapes and
  *    chunk_size give the same bits.
+ *  - After a kernel's first use in the process (which configures it), the
+ *    compute calls make no allocation, synchronisation or configuration
+ *    call, so a sequence of them can be captured in a CUDA graph.  Their
+ *    kernels use programmatic dependent launch: each may start while the
+ *    previous work on `stream` drains, and waits for it before touching
+ *    memory.
  */
 #ifndef LMHEAD_H_
 #define LMHEAD_H_
