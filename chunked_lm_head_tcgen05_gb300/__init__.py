@@ -140,6 +140,28 @@ def _check_tensor(t, name, dtype, shape, allow_none=False):
     del torch
 
 
+def _on_device(tensors, stream, fn):
+    """Run fn() with the tensors' CUDA device current.  The library launches
+    on the current device, so a call whose tensors (or stream) live on
+    another device, or on several, is refused here instead of launched."""
+    import torch
+    devs = {t.device for t in tensors if t is not None}
+    if stream is not None and not isinstance(stream, int) and hasattr(stream, "device"):
+        devs.add(stream.device)
+    if len(devs) > 1:
+        raise ValueError("all tensors and the stream of one call must be on one CUDA device, "
+                         "got %s" % sorted(str(d) for d in devs))
+    if not devs:
+        return fn()
+    with torch.cuda.device(devs.pop()):
+        return fn()
+
+
+def _check_workspace(ws):
+    if ws is None or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+
+
 def lmhead_workspace_size(op, T, H, V, chunk_size):
     return int(library().lmhead_workspace_size(op, T, H, V, chunk_size))
 
@@ -157,10 +179,12 @@ def lmhead_logps_fwd(hidden, weight, targets, loss_mask, temperature, chunk_size
     _check_tensor(logp, "logp", torch.float32, (T,))
     _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
     _check_tensor(lse, "lse", torch.float32, (T,))
-    return int(library().lmhead_logps_fwd(
+    _check_workspace(workspace)
+    tensors = [hidden, weight, targets, loss_mask, logp, entropy, lse, workspace]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_fwd(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
         int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), _stream(stream))))
 
 
 def lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
@@ -180,11 +204,14 @@ def lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size
     _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
     _check_tensor(d_hidden, "d_hidden", torch.float32, (T, H))
     _check_tensor(d_weight, "d_weight", torch.float32, (V, H))
-    return int(library().lmhead_logps_bwd(
+    _check_workspace(workspace)
+    tensors = [hidden, weight, targets, loss_mask, grad_logp, grad_entropy, lse, entropy,
+               d_hidden, d_weight, workspace]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_bwd(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
         int(chunk_size), _ptr(grad_logp), _ptr(grad_entropy), _ptr(lse), _ptr(entropy),
         _ptr(d_hidden), _ptr(d_weight), int(bool(accumulate_dweight)), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), _stream(stream))))
 
 
 def lmhead_logps_fwd_noalloc(hidden, weight, targets, loss_mask, temperature, chunk_size, logp,
@@ -204,9 +231,10 @@ def lmhead_logps_fwd_noalloc(hidden, weight, targets, loss_mask, temperature, ch
     _check_tensor(logp, "logp", torch.float32, (T,))
     _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
     _check_tensor(lse, "lse", torch.float32, (T,))
-    return int(library().lmhead_logps_fwd_noalloc(
+    tensors = [hidden, weight, targets, loss_mask, logp, entropy, lse]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_fwd_noalloc(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
-        int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _stream(stream)))
+        int(chunk_size), _ptr(logp), _ptr(entropy), _ptr(lse), _stream(stream))))
 
 
 def lmhead_logps_fwd_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size, grad_logp,
@@ -227,11 +255,14 @@ def lmhead_logps_fwd_bwd(hidden, weight, targets, loss_mask, temperature, chunk_
     _check_tensor(lse, "lse", torch.float32, (T,))
     _check_tensor(d_hidden, "d_hidden", torch.float32, (T, H))
     _check_tensor(d_weight, "d_weight", torch.float32, (V, H))
-    return int(library().lmhead_logps_fwd_bwd(
+    _check_workspace(workspace)
+    tensors = [hidden, weight, targets, loss_mask, grad_logp, grad_entropy, logp, entropy, lse,
+               d_hidden, d_weight, workspace]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_fwd_bwd(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(loss_mask), T, H, V, float(temperature),
         int(chunk_size), _ptr(grad_logp), _ptr(grad_entropy), _ptr(logp), _ptr(entropy),
         _ptr(lse), _ptr(d_hidden), _ptr(d_weight), int(bool(accumulate_dweight)), int(strategy),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))))
 
 
 def lmhead_fwd_bwd_keeps_logits(T, H, V, chunk_size):
@@ -254,9 +285,10 @@ def lmhead_score_logits_fwd(logits, targets, loss_mask, temperature, logp, entro
     _check_tensor(logp, "logp", torch.float32, (T,))
     _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
     _check_tensor(lse, "lse", torch.float32, (T,))
-    return int(library().lmhead_score_logits_fwd(
+    tensors = [logits, targets, loss_mask, logp, entropy, lse]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_score_logits_fwd(
         _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(logp),
-        _ptr(entropy), _ptr(lse), _stream(stream)))
+        _ptr(entropy), _ptr(lse), _stream(stream))))
 
 
 def lmhead_score_logits_bwd(logits, targets, loss_mask, temperature, grad_logp, grad_entropy,
@@ -272,24 +304,30 @@ def lmhead_score_logits_bwd(logits, targets, loss_mask, temperature, grad_logp, 
     _check_tensor(lse, "lse", torch.float32, (T,))
     _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
     _check_tensor(d_logits, "d_logits", torch.float32, (T, V))
-    return int(library().lmhead_score_logits_bwd(
+    tensors = [logits, targets, loss_mask, grad_logp, grad_entropy, lse, entropy, d_logits]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_score_logits_bwd(
         _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(grad_logp),
-        _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_logits), _stream(stream)))
+        _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_logits), _stream(stream))))
 
 
 def lmhead_selftest_bounded_wait(workspace, limit_ms, stream=None):
     """C ``lmhead_selftest_bounded_wait``; returns the status code of the launch."""
-    return int(library().lmhead_selftest_bounded_wait(
+    _check_workspace(workspace)
+    return _on_device([workspace], stream, lambda: int(library().lmhead_selftest_bounded_wait(
         _ptr(workspace), workspace.numel() * workspace.element_size(), int(limit_ms),
-        _stream(stream)))
+        _stream(stream))))
 
 
 def lmhead_read_device_status(workspace, stream=None):
-    return int(library().lmhead_read_device_status(_ptr(workspace), _stream(stream)))
+    _check_workspace(workspace)
+    return _on_device([workspace], stream, lambda: int(
+        library().lmhead_read_device_status(_ptr(workspace), _stream(stream))))
 
 
 def lmhead_read_scored_count(workspace, stream=None):
-    return int(library().lmhead_read_scored_count(_ptr(workspace), _stream(stream)))
+    _check_workspace(workspace)
+    return _on_device([workspace], stream, lambda: int(
+        library().lmhead_read_scored_count(_ptr(workspace), _stream(stream))))
 
 
 def lmhead_status_string(status):

@@ -30,9 +30,11 @@
  * combined by their log-sum-exp.
  *
  * Conventions shared by every call:
- *  - All tensor pointers are DEVICE pointers owned by the caller.  The
- *    library allocates no device memory, never synchronises the stream in
- *    the compute calls, and enqueues all work on `stream`.
+ *  - All tensor pointers are DEVICE pointers owned by the caller, on the
+ *    current CUDA device, which is where the library launches (the Python
+ *    binding makes the tensors' device current and refuses mixed devices).
+ *    The library allocates no device memory, never synchronises the stream
+ *    in the compute calls, and enqueues all work on `stream`.
  *  - bf16 tensors are passed as raw bfloat16 bit patterns (uint16_t).
  *  - Matrices are row-major and dense: hidden [T, H], weight [V, H],
  *    d_hidden [T, H], d_weight [V, H].
