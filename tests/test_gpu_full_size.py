@@ -139,3 +139,37 @@ def test_device_memory_bounded_by_chunk(case):
     assert peak == after_ws, (peak, after_ws)
     assert peak - base < 2 * T * V, (peak - base, 2 * T * V)
     assert lm.lmhead_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("strategy", ["two_calls", "keep_logits"])
+def test_large_vocabulary_64bit_offsets(strategy):
+    """A 262,144-entry vocabulary at H = 4096: W is 2 GiB and d_weight 4 GiB, so
+    byte offsets pass 2^32 and element offsets approach 2^30.  Sampled rows
+    and, with cotangents on a token sample, the whole d_weight (its last rows
+    included) against the oracle, for the two-call path and for the single
+    call with kept logits."""
+    import chunked_lm_head_tcgen05_gb300 as lm
+    from gpu_helpers import run_gpu_fwd_bwd
+    w = W.WORKLOADS["tiny"].with_(T=700, H=4096, V=262144, chunk_size=2048, temperature=0.9,
+                                  mask="bernoulli", mask_drop=0.25, hidden_dist="rms",
+                                  weight_std=0.02, seed=51)
+    x = W.make_inputs(w)
+    rows, _ = _sample_rows(x, 5, 0, 4)
+    keepmask = torch.zeros(w.T)
+    keepmask[torch.from_numpy(rows)] = 1.0
+    x["grad_logp"] = x["grad_logp"] * keepmask
+    x["grad_entropy"] = x["grad_entropy"] * keepmask
+    if strategy == "two_calls":
+        g = run_gpu(x)
+        assert g["fwd_status"] == 0 and g["bwd_status"] == 0
+    else:
+        g = run_gpu_fwd_bwd(x, lm.LMHEAD_STRATEGY_KEEP_LOGITS)
+        assert g["status"] == 0
+    o = run_oracle(x, rows=rows)
+    e = assert_parity(g, o, rows=rows, keys=("logp", "entropy", "lse"))
+    e["d_weight"] = rel_fro(g["d_weight"], o["d_weight"])
+    e["d_hidden"] = rel_fro(g["d_hidden"][rows], o["d_hidden"])
+    e["d_weight_tail"] = rel_fro(g["d_weight"][-4096:], o["d_weight"][-4096:])
+    assert max(e["d_weight"], e["d_weight_tail"]) <= LIMITS["d_weight"], e
+    assert e["d_hidden"] <= LIMITS["d_hidden"], e
+    print(strategy, e)
