@@ -205,3 +205,41 @@ def test_extreme_temperatures_and_peaked_distributions(tau, wstd):
     else:
         assert np.median(o["entropy"][m]) < 2.0
     print(tau, wstd, e)
+
+
+def test_soak_back_to_back_steps_bitwise():
+    """Forty forward + backward steps back to back on one stream (each kernel
+    may start while its predecessor drains and must wait before touching its
+    inputs): every step's outputs equal the first step's bit for bit."""
+    ensure_built()
+    w = _w(1500, 256, 4000, 64, 0.8, "bernoulli", mask_drop=0.3, hidden_dist="rms", seed=61)
+    x = W.make_inputs(w)
+    g = to_device(x)
+    T, H = g["hidden"].shape
+    V = g["weight"].shape[0]
+    c, tau = x["chunk_size"], x["temperature"]
+    ws = torch.empty(max(lm.lmhead_workspace_size(0, T, H, V, c),
+                         lm.lmhead_workspace_size(1, T, H, V, c)), dtype=torch.uint8,
+                     device="cuda")
+    out = {k: torch.empty(T, device="cuda") for k in ("logp", "entropy", "lse")}
+    out["d_hidden"] = torch.empty((T, H), device="cuda")
+    out["d_weight"] = torch.empty((V, H), device="cuda")
+    first = None
+    mismatches = []
+    for i in range(40):
+        rc = lm.lmhead_logps_fwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau, c,
+                                 out["logp"], out["entropy"], out["lse"], ws)
+        rc |= lm.lmhead_logps_bwd(g["hidden"], g["weight"], g["targets"], g["loss_mask"], tau,
+                                  c, g["grad_logp"], g["grad_entropy"], out["lse"],
+                                  out["entropy"], out["d_hidden"], out["d_weight"], 0, ws)
+        assert rc == 0
+        snap = {k: v.clone() for k, v in out.items()}   # stream-ordered copies
+        if first is None:
+            first = snap
+        else:
+            for k in out:
+                if not torch.equal(snap[k], first[k]):
+                    mismatches.append((i, k))
+    torch.cuda.synchronize()
+    assert lm.lmhead_read_device_status(ws) == 0
+    assert not mismatches, mismatches[:10]
