@@ -35,6 +35,8 @@
 // other CTAs poll, so the whole grid winds down.
 #include "tc_gemm.cuh"
 
+#include <type_traits>
+
 namespace lmh {
 namespace {
 
@@ -320,52 +322,62 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         const int mrow = x.m * PAIR_M + r128;   // this CTA's first M row (or M column)
         const int ncol = x.n * BN + r128;       // this CTA's half of the N tile
-        for (int kb = 0; kb < x.kblocks; ++kb) {
-          if (!dz_ready && kb % (BN / BK) == 0) {
-            if (ld_acquire_gpu(F.dz_all(x.b)) >= dz_target) {
-              dz_ready = true;
-            } else if (!wait_flag(F.dz_col(x.b, kb / (BN / BK)), 2 * x.k.mt, abort, st)) {
+        // The K loop is compiled once per tile kind: a kind test inside it costs
+        // this TMA-issue-bound thread about a tenth of the kernel's speed.
+        auto produce = [&](auto kind_tag) {
+          constexpr int KIND = decltype(kind_tag)::value;
+          for (int kb = 0; kb < x.kblocks; ++kb) {
+            if constexpr (KIND == U_DH) {
+              if (!dz_ready && kb % (BN / BK) == 0) {
+                if (ld_acquire_gpu(F.dz_all(x.b)) >= dz_target) {
+                  dz_ready = true;
+                } else if (!wait_flag(F.dz_col(x.b, kb / (BN / BK)), 2 * x.k.mt, abort, st)) {
+                  ok = false;
+                  break;
+                }
+                fence_async_global();
+              }
+            }
+            if (leader && ahead < 0 && kb == max(0, x.kblocks - FETCH_AHEAD_KB))
+              ahead = atomicAdd(A.unit_counter, 1);
+            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, st)) {
               ok = false;
               break;
             }
-            fence_async_global();
+            const uint32_t fb_local = smem_addr(&ctl->full[stage]);
+            if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * 2);
+            const uint32_t fb = map_to_cta(fb_local, 0);
+            const uint32_t sa = smem_base + stage * C::STAGE;
+            const uint32_t sb = sa + A_TILE_BYTES;
+            const int k0 = kb * BK;
+            if constexpr (KIND == U_DZ) {
+              tma_load_2d_pair(sa, &A.h_k, fb, k0, x.k.t0 + mrow);
+              tma_load_2d_pair(sb, &A.w_k, fb, k0, x.k.v0 + ncol);
+            } else if constexpr (KIND == U_DH) {
+              tma_load_2d_pair(sa, &A.dz_k, fb, k0, mrow);
+              tma_load_3d_pair(sb, &A.w_mn, fb, 0, x.k.v0 + k0, ncol / 64);
+            } else {
+              tma_load_3d_pair(sa, &A.dz_mn, fb, 0, k0, mrow / 64);
+              tma_load_3d_pair(sb, &A.h_mn, fb, 0, x.k.t0 + k0, ncol / 64);
+            }
+            if (++stage == C::NSTAGE) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          if (leader && ahead < 0 && kb == max(0, x.kblocks - FETCH_AHEAD_KB))
-            ahead = atomicAdd(A.unit_counter, 1);
-          if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, st)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb_local = smem_addr(&ctl->full[stage]);
-          if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * 2);
-          const uint32_t fb = map_to_cta(fb_local, 0);
-          const uint32_t sa = smem_base + stage * C::STAGE;
-          const uint32_t sb = sa + A_TILE_BYTES;
-          const int k0 = kb * BK;
-          if (x.kind == U_DZ) {
-            tma_load_2d_pair(sa, &A.h_k, fb, k0, x.k.t0 + mrow);
-            tma_load_2d_pair(sb, &A.w_k, fb, k0, x.k.v0 + ncol);
-          } else if (x.kind == U_DH) {
-            tma_load_2d_pair(sa, &A.dz_k, fb, k0, mrow);
-            tma_load_3d_pair(sb, &A.w_mn, fb, 0, x.k.v0 + k0, ncol / 64);
-          } else {
-            tma_load_3d_pair(sa, &A.dz_mn, fb, 0, k0, mrow / 64);
-            tma_load_3d_pair(sb, &A.h_mn, fb, 0, x.k.t0 + k0, ncol / 64);
-          }
-          if (++stage == C::NSTAGE) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        };
+        if (x.kind == U_DZ)
+          produce(std::integral_constant<int, U_DZ>{});
+        else if (x.kind == U_DH)
+          produce(std::integral_constant<int, U_DH>{});
+        else
+          produce(std::integral_constant<int, U_DW>{});
       }
       if (!ok) pause_ns(100000);   // let copies already issued land before exit
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t ID_DZ = idesc_bf16_f32(PAIR_M, BN, false, false);
-      constexpr uint32_t ID_DH = idesc_bf16_f32(PAIR_M, BN, false, true);
-      constexpr uint32_t ID_DW = idesc_bf16_f32(PAIR_M, BN, true, true);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int i = 0; ok; ++i) {
@@ -380,39 +392,48 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (u < 0) break;
         const Unit x = decode(A, tb_prefix, scored, ht, u);
         if (x.kblocks == 0) continue;
-        const bool a_mn = x.kind == U_DW;
-        const bool b_mn = x.kind != U_DZ;
-        const uint32_t idesc = x.kind == U_DZ ? ID_DZ : (x.kind == U_DH ? ID_DH : ID_DW);
         if (!wait_bar(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, st)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < x.kblocks; ++kb) {
-          if (!wait_bar(smem_addr(&ctl->full[stage]), phase, abort, st)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t sa = smem_base + stage * C::STAGE;
-          const uint32_t sb = sa + A_TILE_BYTES;
+        // one K loop per tile kind, operand layouts and descriptor fixed at compile time
+        auto issue = [&](auto kind_tag) {
+          constexpr int KIND = decltype(kind_tag)::value;
+          constexpr bool AMN = KIND == U_DW, BMN = KIND != U_DZ;
+          constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, AMN, BMN);
+          for (int kb = 0; kb < x.kblocks; ++kb) {
+            if (!wait_bar(smem_addr(&ctl->full[stage]), phase, abort, st)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sa = smem_base + stage * C::STAGE;
+            const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // K-major: 16 more K elements are 32 bytes along the swizzled row;
-            // MN-major: 16 more K rows are 2 KB further, 64-wide MN chunks 8 KB apart.
-            const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                     : smem_desc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                     : smem_desc_sw128(sb + k * 32, 16, 1024);
-            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: 16 more K elements are 32 bytes along the swizzled row;
+              // MN-major: 16 more K rows are 2 KB further, 64-wide MN chunks 8 KB apart.
+              const uint64_t ad = AMN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd = BMN ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+            }
+            umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+            if (++stage == C::NSTAGE) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
-          if (++stage == C::NSTAGE) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
+        };
+        if (x.kind == U_DZ)
+          issue(std::integral_constant<int, U_DZ>{});
+        else if (x.kind == U_DH)
+          issue(std::integral_constant<int, U_DH>{});
+        else
+          issue(std::integral_constant<int, U_DW>{});
         if (!ok) break;
         umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
         acc ^= 1;

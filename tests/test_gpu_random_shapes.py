@@ -3,8 +3,8 @@ vocabulary sizes, chunk sizes, temperatures, mask styles, missing
 cotangents and d_weight accumulation drawn together, at sizes the oracle
 finishes in about a second each.  Each case also runs the single-call path
 with kept logits (the fp16 logit store and in-place cotangent pass) against
-the oracle, and every fourth case the opt-in single-kernel backward forms,
-which must give the default path's bits."""
+the oracle, and every fourth case the other backward forms (two launches per
+block, launch windows), which must give the default path's bits."""
 import os
 
 import numpy as np
@@ -63,7 +63,7 @@ def test_random_configuration(i):
     if i % 4 == 0:
         old = os.environ.get("LMHEAD_BWD_PERSISTENT")
         try:
-            for mode in ("1", "2"):
+            for mode in ("0", "2"):
                 os.environ["LMHEAD_BWD_PERSISTENT"] = mode
                 g2 = run_gpu(x, grad_entropy=opts["grad_entropy"], accumulate=opts["accumulate"],
                              d_weight_init=init)
