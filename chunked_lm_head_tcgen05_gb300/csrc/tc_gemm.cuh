@@ -42,6 +42,7 @@
 
 #include <atomic>
 #include <climits>
+#include <type_traits>
 
 namespace lmh {
 
@@ -312,53 +313,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (s.k_blocks == 0) continue;
         const CUtensorMap* ma = &L.map_a[q];
         const CUtensorMap* mb = &L.map_b[q];
-        const bool a_mn = L.prob[q].a_mn != 0;
-        int m, split, nb, ne;
-        s.unit(lu, m, split, nb, ne);
-        const int arow = m * C::UNIT_M + static_cast<int>(rank) * BM;
-        for (int n = nb; ok && n < ne; ++n) {
-          const int bcol = n * BN + static_cast<int>(rank) * C::B_ROWS;
-          for (int kb = 0; kb < s.k_blocks; ++kb) {
-            if (leader && ahead < 0 && n == ne - 1 && kb == max(0, s.k_blocks - FETCH_AHEAD_KB))
-              ahead = atomicAdd(L.counter, 1);
-            if (!wait_bounded<PAIR>(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb_local = smem_addr(&ctl->full[stage]);
-            if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * C::CTAS);
-            const uint32_t sa = smem_base + stage * C::STAGE;
-            const uint32_t sb = sa + A_TILE_BYTES;
-            // MN-major operands use 3-D maps (64 elements, K rows, 64-element
-            // chunks): one instruction loads all of this CTA's chunks
-            if constexpr (PAIR) {
-              const uint32_t fb = map_to_cta(fb_local, 0);
-              if (!a_mn)
-                tma_load_2d_pair(sa, ma, fb, kb * BK, arow);
-              else
-                tma_load_3d_pair(sa, ma, fb, 0, kb * BK, arow / 64);
-              if (!B_MN)
-                tma_load_2d_pair(sb, mb, fb, kb * BK, bcol);
-              else
-                tma_load_3d_pair(sb, mb, fb, 0, kb * BK, bcol / 64);
-            } else {
-              if (!a_mn)
-                tma_load_2d(sa, ma, fb_local, kb * BK, arow);
-              else
-                tma_load_3d(sa, ma, fb_local, 0, kb * BK, arow / 64);
-              if (!B_MN)
-                tma_load_2d(sb, mb, fb_local, kb * BK, bcol);
-              else
-                tma_load_3d(sb, mb, fb_local, 0, kb * BK, bcol / 64);
-            }
-            issued_mask |= 1u << stage;
-            issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == C::NSTAGE) {
-              stage = 0;
-              phase ^= 1;
+        // the A layout is fixed per problem: the K loop is compiled for each
+        // so that no per-step test of it is left in the issue path
+        auto produce = [&](auto amn_tag) {
+          constexpr bool A_MN = decltype(amn_tag)::value;
+          int m, split, nb, ne;
+          s.unit(lu, m, split, nb, ne);
+          const int arow = m * C::UNIT_M + static_cast<int>(rank) * BM;
+          for (int n = nb; ok && n < ne; ++n) {
+            const int bcol = n * BN + static_cast<int>(rank) * C::B_ROWS;
+            for (int kb = 0; kb < s.k_blocks; ++kb) {
+              if (leader && ahead < 0 && n == ne - 1 && kb == max(0, s.k_blocks - FETCH_AHEAD_KB))
+                ahead = atomicAdd(L.counter, 1);
+              if (!wait_bounded<PAIR>(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb_local = smem_addr(&ctl->full[stage]);
+              if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * C::CTAS);
+              const uint32_t sa = smem_base + stage * C::STAGE;
+              const uint32_t sb = sa + A_TILE_BYTES;
+              // MN-major operands use 3-D maps (64 elements, K rows, 64-element
+              // chunks): one instruction loads all of this CTA's chunks
+              if constexpr (PAIR) {
+                const uint32_t fb = map_to_cta(fb_local, 0);
+                if constexpr (!A_MN)
+                  tma_load_2d_pair(sa, ma, fb, kb * BK, arow);
+                else
+                  tma_load_3d_pair(sa, ma, fb, 0, kb * BK, arow / 64);
+                if constexpr (!B_MN)
+                  tma_load_2d_pair(sb, mb, fb, kb * BK, bcol);
+                else
+                  tma_load_3d_pair(sb, mb, fb, 0, kb * BK, bcol / 64);
+              } else {
+                if constexpr (!A_MN)
+                  tma_load_2d(sa, ma, fb_local, kb * BK, arow);
+                else
+                  tma_load_3d(sa, ma, fb_local, 0, kb * BK, arow / 64);
+                if constexpr (!B_MN)
+                  tma_load_2d(sb, mb, fb_local, kb * BK, bcol);
+                else
+                  tma_load_3d(sb, mb, fb_local, 0, kb * BK, bcol / 64);
+              }
+              issued_mask |= 1u << stage;
+              issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+              if (++stage == C::NSTAGE) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
           }
-        }
+        };
+        if (L.prob[q].a_mn != 0)
+          produce(std::true_type{});
+        else
+          produce(std::false_type{});
       }
       if (!ok) {
         if constexpr (PAIR) {
@@ -373,8 +382,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t IDESC_AK = idesc_bf16_f32(C::UNIT_M, BN, false, B_MN);
-      constexpr uint32_t IDESC_AMN = idesc_bf16_f32(C::UNIT_M, BN, true, B_MN);
       constexpr uint32_t B_LBO = 8192;   // MN-major: the 64-wide N chunks are 8 KB apart
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -392,56 +399,62 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int lu = split_unit(sc0, u, q);
         const Sched s = q ? sc1 : sc0;
         if (s.k_blocks == 0) continue;
-        const bool a_mn = L.prob[q].a_mn != 0;
-        const uint32_t idesc = a_mn ? IDESC_AMN : IDESC_AK;
-        int m, split, nb, ne;
-        s.unit(lu, m, split, nb, ne);
-        for (int n = nb; ok && n < ne; ++n) {
-          if (!wait_bounded<PAIR>(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t d_tmem = tmem_base + acc * BN;
-          for (int kb = 0; kb < s.k_blocks; ++kb) {
-            if (!wait_bounded<PAIR>(smem_addr(&ctl->full[stage]), phase, abort, status)) {
+        auto issue = [&](auto amn_tag) {
+          constexpr bool A_MN = decltype(amn_tag)::value;
+          constexpr uint32_t IDESC = idesc_bf16_f32(C::UNIT_M, BN, A_MN, B_MN);
+          int m, split, nb, ne;
+          s.unit(lu, m, split, nb, ne);
+          for (int n = nb; ok && n < ne; ++n) {
+            if (!wait_bounded<PAIR>(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, status)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const uint32_t sa = smem_base + stage * C::STAGE;
-            const uint32_t sb = sa + A_TILE_BYTES;
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int kb = 0; kb < s.k_blocks; ++kb) {
+              if (!wait_bounded<PAIR>(smem_addr(&ctl->full[stage]), phase, abort, status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              const uint32_t sa = smem_base + stage * C::STAGE;
+              const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              // K-major: the next 16 K elements are 32 bytes further along the
-              // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further,
-              // with the 64-wide MN chunks 8 KB apart.
-              const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
-              const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, B_LBO, 1024)
-                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
+              for (int k = 0; k < BK / 16; ++k) {
+                // K-major: the next 16 K elements are 32 bytes further along the
+                // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further,
+                // with the 64-wide MN chunks 8 KB apart.
+                const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                         : smem_desc_sw128(sa + k * 32, 16, 1024);
+                const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, B_LBO, 1024)
+                                         : smem_desc_sw128(sb + k * 32, 16, 1024);
+                if constexpr (PAIR)
+                  umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                else
+                  umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              }
               if constexpr (PAIR)
-                umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
               else
-                umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                umma_commit(smem_addr(&ctl->empty[stage]));
+              if (++stage == C::NSTAGE) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
+            if (!ok) break;
             if constexpr (PAIR)
-              umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
+              umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
             else
-              umma_commit(smem_addr(&ctl->empty[stage]));
-            if (++stage == C::NSTAGE) {
-              stage = 0;
-              phase ^= 1;
-            }
+              umma_commit(smem_addr(&ctl->tfull[acc]));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
           }
-          if (!ok) break;
-          if constexpr (PAIR)
-            umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
-          else
-            umma_commit(smem_addr(&ctl->tfull[acc]));
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
-        }
+        };
+        if (L.prob[q].a_mn != 0)
+          issue(std::true_type{});
+        else
+          issue(std::false_type{});
       }
       if (!ok) {
         if constexpr (PAIR) {
