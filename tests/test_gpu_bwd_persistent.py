@@ -147,3 +147,21 @@ def test_persistent_full_size_qwen3_4b_bitwise():
     x = W.make_inputs(W.WORKLOADS["qwen3_4b"])
     a, b = _both(x)
     _same_bits(a, b)
+
+
+def test_more_token_blocks_than_the_flags_hold_fall_back_to_per_block():
+    """With 257 token blocks (chunk 1 keeps the blocks at 256 x 256) the
+    persistent kernel's flag layout does not apply: the default mode must
+    take the per-block path, and the result must still match the oracle."""
+    x = W.make_inputs(_w(65792, 64, 512, 1, 0.9, "bernoulli", mask_drop=0.25, seed=21))
+    n_tb, n_vb, tb, vb = _blocks(x)
+    assert n_tb > 255 and tb == 256
+    old = os.environ.pop("LMHEAD_BWD_PERSISTENT", None)
+    try:
+        g, names = _kernels(lambda: run_gpu(x))
+    finally:
+        if old is not None:
+            os.environ["LMHEAD_BWD_PERSISTENT"] = old
+    assert "bwd_dz_gemm" in names and "bwd_all_gemm" not in names, names
+    assert g["fwd_status"] == 0 and g["bwd_status"] == 0
+    assert_parity(g, run_oracle(x))
