@@ -34,6 +34,8 @@ UNIT = "tokens/s"
 # GEMM kernels and their algorithmic flops per step in units of T_v*H*V
 GEMM_KERNELS = {"fwd_stats_gemm": 2.0, "bwd_dz_gemm": 2.0, "bwd_grad_gemm": 4.0,
                 "bwd_all_gemm": 6.0, "bwd_window_gemm": 6.0}
+# the part of those flops that recomputes the forward's logits
+RECOMPUTE = {"bwd_dz_gemm": 2.0, "bwd_all_gemm": 2.0, "bwd_window_gemm": 2.0}
 
 
 def parse():
@@ -340,7 +342,9 @@ def run_ours(args, rank, world, local):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(dom, args.workload),
                 "peak_source": "%s bf16_tflops_sustained (of %s)" % ("MEASURED_PEAKS.json", src),
-                "flops_per_launch": flops_per_launch, "launches_per_step": launches_per_step}
+                "flops_per_launch": flops_per_launch, "launches_per_step": launches_per_step,
+                "frac_without_recompute": achieved / peak
+                * (GEMM_KERNELS[dom] - RECOMPUTE.get(dom, 0.0)) / GEMM_KERNELS[dom]}
     kernels = {k: {"launches_per_step": v[0] / n_prof_steps, "ms_per_step": v[1] / n_prof_steps,
                    "share": v[1] / total_ms} for k, v in sorted(per.items())}
 
