@@ -97,9 +97,9 @@ bool use_pair() {
 
 // Backward launch structure, from LMHEAD_BWD_PERSISTENT (read on every call
 // so that the forms can be compared in one process; all give the same bits):
-//   unset or 1  one persistent launch for all blocks, tiles ordered by
-//               completion flags (the default; 7.5% faster than two launches
-//               per block on the Qwen3-4B-sized backward, equal elsewhere);
+//   unset       chosen by block size (below);
+//   1           one persistent launch for all blocks, tiles ordered by
+//               completion flags;
 //   0           two launches per block (dz, then dh + dW);
 //   2           windows: blocks + 1 launches, each a block's dh + dW tiles
 //               followed by the next block's dz tiles.
@@ -107,8 +107,21 @@ bool use_pair() {
 // token blocks; otherwise the backward runs as two launches per block.
 int bwd_mode() {
   const char* e = std::getenv("LMHEAD_BWD_PERSISTENT");
-  if (!e || !e[0]) return 1;
+  if (!e || !e[0]) return -1;
   return e[0] == '0' ? 0 : (e[0] == '2' ? 2 : 1);
+}
+
+// Unset mode: the persistent launch removes two launch boundaries and their
+// tails per block, which pays while blocks are small (Qwen3-4B-sized head,
+// 4096 x 16896 x 2560 MACs per block: 5.55 vs 5.86 ms).  With blocks of
+// 1e12 MACs and more (chunk 4096 on a 61k-token row or a 200,000-token
+// trace) the boundaries cost under 1% and the persistent launch measured
+// 1.0-1.3% slower than two launches per block, so those take the latter.
+constexpr double kPersistentMaxBlockMacs = 5e11;
+
+bool persistent_pays(int64_t Tb, int64_t Vb, int64_t H) {
+  return static_cast<double>(Tb) * static_cast<double>(Vb) * static_cast<double>(H) <=
+         kPersistentMaxBlockMacs;
 }
 
 int unit_rows() { return use_pair() ? 2 * BM : BM; }
@@ -228,16 +241,25 @@ struct BwdPlan {
 };
 
 // Backward blocks T_b x V_b with T_b * V_b <= chunk_size * V (the scratch
-// bound); T_b ~ V_b ~ sqrt(chunk_size * V) minimises the fp32
-// read-modify-write traffic of dh and dW, 8 T V H (1/T_b + 1/V_b) bytes.
+// bound).  T_b ~ V_b ~ sqrt(chunk_size * V) would minimise the fp32
+// read-modify-write traffic of dh and dW, 8 T V H (1/T_b + 1/V_b) bytes, but
+// a token block's hidden rows are read again for every dz column tile and
+// every dW tile, so T_b is also capped to keep them (T_b x H bf16) within
+// kHiddenBlockBytes of L2; V_b then takes the rest of the bound.  On a
+// 200,000-token trace (H 2048) and a 61k-token row (H 4096) at chunk 4096
+// the cap makes the backward 6-8% faster than square blocks; where the
+// square block is already small enough (H 2560 at chunk 512) nothing changes.
 // T_b is a multiple of 256 rows (one CTA pair's tile), V_b of 256 columns.
-BwdPlan plan_bwd(int64_t T, int64_t V, int64_t chunk) {
+constexpr int64_t kHiddenBlockBytes = 40ll << 20;
+
+BwdPlan plan_bwd(int64_t T, int64_t H, int64_t V, int64_t chunk) {
   BwdPlan p;
   constexpr int64_t TU = 2 * BM;
   const int64_t T_alloc = round_up(T, BM);
   const int64_t V_pad = round_up(V, BN);
   const double S = static_cast<double>(chunk) * static_cast<double>(V);
   int64_t tb_max = static_cast<int64_t>(std::floor(std::sqrt(S) / TU)) * TU;
+  tb_max = std::min<int64_t>(tb_max, kHiddenBlockBytes / (2 * H) / TU * TU);
   tb_max = std::max<int64_t>(TU, std::min<int64_t>(tb_max, round_up(T_alloc, TU)));
   p.n_tb = ceil_div(T_alloc, tb_max);
   p.Tb = round_up(ceil_div(T_alloc, p.n_tb), TU);
@@ -272,7 +294,7 @@ FusedPlan plan_fused(int64_t T, int64_t H, int64_t V, int64_t chunk) {
   tb = std::max<int64_t>(unit, std::min<int64_t>(tb, round_up(T_alloc, unit)));
   p.Tb = tb;
   p.n_tb = ceil_div(T_alloc, tb);
-  const BwdPlan bp = plan_bwd(T, V, chunk);
+  const BwdPlan bp = plan_bwd(T, H, V, chunk);
   const double flops_rate = 1.6e15, bytes_rate = 5.0e12;   // GB300 sustained, rounded down
   const double TVd = static_cast<double>(T) * static_cast<double>(V);
   const double dw_pass = 8.0 * static_cast<double>(V) * static_cast<double>(H) / bytes_rate;
@@ -303,7 +325,7 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
   } else if (op == LMHEAD_OP_BWD) {
     // two unit counters per block (per-block launches), or one counter and
     // the tile completion flags of the persistent launch
-    const BwdPlan bp = plan_bwd(T, V, chunk);
+    const BwdPlan bp = plan_bwd(T, H, V, chunk);
     const int64_t blocks = bp.n_tb * bp.n_vb;
     L.n_counters =
         std::max<int64_t>(2 * blocks, (blocks + 1) + blocks * (1 + bp.Tb / (2 * BM) + 2 * bp.Vb / BN));
@@ -318,7 +340,7 @@ Layout layout(int op, int64_t T, int64_t H, int64_t V, int64_t chunk) {
   if (op == LMHEAD_OP_FWD) {
     L.part = take(16 * static_cast<size_t>(kMaxSplits) * static_cast<size_t>(T_alloc));
   } else if (op == LMHEAD_OP_BWD) {
-    const BwdPlan bp = plan_bwd(T, V, chunk);
+    const BwdPlan bp = plan_bwd(T, H, V, chunk);
     L.coef = take(16 * static_cast<size_t>(T_alloc));
     L.dz = take(2 * static_cast<size_t>(bp.Tb) * static_cast<size_t>(bp.Vb));
   } else {
@@ -429,7 +451,7 @@ lmhead_status lmhead_plan_info(int64_t T, int32_t H, int32_t V, int32_t chunk_si
     *fwd_splits = sms > 0 ? choose_splits(ceil_div(T, unit_rows()), ceil_div(V, BN),
                                           use_pair() ? sms / 2 : sms)
                           : 0;
-  const BwdPlan bp = plan_bwd(T, V, chunk_size);
+  const BwdPlan bp = plan_bwd(T, H, V, chunk_size);
   if (bwd_tokens) *bwd_tokens = static_cast<int32_t>(bp.Tb);
   if (bwd_vocab) *bwd_vocab = static_cast<int32_t>(bp.Vb);
   return LMHEAD_OK;
@@ -539,13 +561,14 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
     }));
   }
 
-  const BwdPlan bp = plan_bwd(T, V, chunk_size);
+  const BwdPlan bp = plan_bwd(T, H, V, chunk_size);
   const float scale = kLog2e / temperature;
   const bool pair = use_pair();
   const int64_t um = unit_rows();
   const int64_t ctas = pair ? 2 : 1;
 
-  const int mode = bwd_mode();
+  int mode = bwd_mode();
+  if (mode < 0) mode = persistent_pays(bp.Tb, bp.Vb, H) ? 1 : 0;
   if (pair && mode != 0 && bp.n_tb <= BWD_ALL_MAX_TOKEN_BLOCKS) {
     // every block's dz, dh and dW tiles in one launch, ordered by tile flags
     BwdAllArgs a;
