@@ -78,6 +78,9 @@ struct GemmArgs {
   float* m_tile;         // EPI_FWD_Z: [rows][m_tile_ld] reference max of each 256-column tile
   int m_tile_ld;
   int n_fastest;         // unit order: 1 = N tiles of one M block consecutively (one tile per unit)
+  int m_group;           // unit order otherwise: M blocks fastest, taken in groups of m_group
+                         // blocks that run through every N split before the next group
+                         // starts (0 = all M blocks in one group)
   int out_mode;          // 0: per-thread global stores; 1: TMA store of map_out tiles;
                          // 2: TMA reduce-add into map_out (EPI_STORE_F32 accumulation)
 };

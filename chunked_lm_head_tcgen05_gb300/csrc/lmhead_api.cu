@@ -272,6 +272,35 @@ BwdPlan plan_bwd(int64_t T, int64_t H, int64_t V, int64_t chunk) {
   return p;
 }
 
+// Forward unit order.  The forward's units (token block, vocabulary split)
+// are handed out token-block fastest, so the CTAs running at one time sweep
+// the same split's W tiles together (one DRAM read, the rest L2 hits) while
+// each re-reads its own token block's hidden rows (256 x H bf16) once per
+// 256-column vocabulary tile.  With every SM on a different token block
+// those rows alone can outgrow L2 (76 pairs x 256 rows x 4096 x 2 B =
+// 152 MB at H = 4096), and then the re-reads go to DRAM.  So token blocks
+// are taken in groups whose hidden rows fit in kFwdGroupBytes (a quarter of
+// L2); a group runs through all splits before the next one starts, which
+// costs one more read of W per group (a few hundred GB/s at most).
+// Measured on GB300, forward alone, interleaved against the plain order:
+// 61k-token row at H = 4096 -10 to -15%, 45k scored tokens at H = 2560
+// -3 to -4%, 160k at H = 2048 -1 to -2%, for any budget from 20 to 48 MB;
+// 16 token blocks at H = 2560 (4096 tokens) fit in one group (unchanged).
+// LMHEAD_FWD_GROUP_MB, read on every call, overrides the budget (0: one
+// group, the plain order); the order changes no result bit, since every
+// unit is computed whole by one CTA pair.
+constexpr int64_t kFwdGroupBytes = 32ll << 20;
+
+int fwd_m_group(int64_t H) {
+  int64_t budget = kFwdGroupBytes;
+  if (const char* e = std::getenv("LMHEAD_FWD_GROUP_MB"); e && e[0]) {
+    budget = std::atoll(e) << 20;
+    if (budget <= 0) return 0;
+  }
+  const int64_t panel = static_cast<int64_t>(unit_rows()) * 2 * H;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(budget / panel, 1 << 20)));
+}
+
 // Single-call forward + backward that keeps each token block's logits over
 // the whole vocabulary (T_b x V_pad 16-bit values <= chunk_size x V) instead
 // of recomputing them.  It pays when the recompute GEMM (2 T H V flops)
@@ -496,6 +525,7 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   p.dyn_base = 0;
   p.dev_rows = &f.st->rows;
   p.n_splits = splits;
+  p.m_group = fwd_m_group(H);
   p.status = &f.st->status;
   p.scale = kLog2e / temperature;
   p.y_c = f.y_c;
@@ -807,6 +837,7 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
     pf.dyn_base = static_cast<int>(t0);
     pf.dev_rows = &f.st->rows;
     pf.n_splits = splits;
+    pf.m_group = fwd_m_group(H);
     pf.status = &f.st->status;
     pf.scale = scale;
     pf.row_base = static_cast<int>(t0);

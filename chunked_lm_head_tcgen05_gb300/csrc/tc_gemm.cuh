@@ -120,7 +120,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 }
 
 struct Sched {
-  int M, K, m_tiles, n_tiles, n_splits, k_blocks, units, n_fastest;
+  int M, K, m_tiles, n_tiles, n_splits, k_blocks, units, n_fastest, m_group;
 
   __device__ __forceinline__ void init(const GemmArgs& p, int unit_m) {
     int dev = 0;
@@ -134,17 +134,26 @@ struct Sched {
     k_blocks = (K + BK - 1) / BK;
     units = m_tiles * n_splits;
     n_fastest = p.n_fastest && n_splits == n_tiles;
+    m_group = (p.m_group > 0 && p.m_group < m_tiles) ? p.m_group : m_tiles;
   }
 
   // Unit u -> M block m and N tiles [nb, ne).  M-fastest order lets units
-  // that run together share the B panel; N-fastest lets them share A.
+  // that run together share the B panel; N-fastest lets them share A.  In
+  // M-fastest order the M blocks are taken m_group at a time: a group's
+  // units (its blocks x every split) are numbered before the next group's,
+  // so the A panels in use at once stay within m_group blocks (the last
+  // group may be smaller).  With one group this is plain M-fastest order.
   __device__ __forceinline__ void unit(int u, int& m, int& split, int& nb, int& ne) const {
     if (n_fastest) {
       m = u / n_splits;
       split = u - m * n_splits;
     } else {
-      m = u % m_tiles;
-      split = u / m_tiles;
+      const int per_group = m_group * n_splits;
+      const int m0 = (u / per_group) * m_group;
+      const int gm = min(m_group, m_tiles - m0);
+      const int r = u - (m0 / m_group) * per_group;
+      split = r / gm;
+      m = m0 + (r - split * gm);
     }
     nb = static_cast<int>(static_cast<long long>(split) * n_tiles / n_splits);
     ne = static_cast<int>(static_cast<long long>(split + 1) * n_tiles / n_splits);

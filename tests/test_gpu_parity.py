@@ -243,3 +243,30 @@ def test_soak_back_to_back_steps_bitwise():
     torch.cuda.synchronize()
     assert lm.lmhead_read_device_status(ws) == 0
     assert not mismatches, mismatches[:10]
+
+
+def test_forward_token_block_groups():
+    """The forward hands out its (token block, vocabulary split) units in
+    groups of token blocks; the grouping changes which units run together,
+    never a result bit.  A 1 MB budget at H = 512 gives groups of 4 blocks
+    of 256 rows over 10 blocks (4, 4, then a ragged 2), which must match the
+    plain order bitwise and the oracle within the tolerances."""
+    import os
+    w = _w(2500, 512, 3000, 64, 0.8, "bernoulli", mask_drop=0.15, hidden_dist="rms",
+           weight_std=0.05)
+    x = W.make_inputs(w)
+    old = os.environ.get("LMHEAD_FWD_GROUP_MB")
+    try:
+        os.environ["LMHEAD_FWD_GROUP_MB"] = "0"
+        plain = run_gpu(x, backward=False)
+        os.environ["LMHEAD_FWD_GROUP_MB"] = "1"
+        grouped = run_gpu(x, backward=False)
+    finally:
+        if old is None:
+            os.environ.pop("LMHEAD_FWD_GROUP_MB", None)
+        else:
+            os.environ["LMHEAD_FWD_GROUP_MB"] = old
+    for k in ("logp", "entropy", "lse"):
+        assert np.array_equal(grouped[k], plain[k]), k
+    assert grouped["fwd_status"] == 0
+    assert_parity(grouped, run_oracle(x, backward=False), keys=("logp", "entropy", "lse"))
