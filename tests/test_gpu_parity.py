@@ -270,3 +270,23 @@ def test_forward_token_block_groups():
         assert np.array_equal(grouped[k], plain[k]), k
     assert grouped["fwd_status"] == 0
     assert_parity(grouped, run_oracle(x, backward=False), keys=("logp", "entropy", "lse"))
+
+
+@pytest.mark.parametrize("H", [8192, 16384])
+def test_wide_hidden(H):
+    """Hidden sizes of large-model heads: long K loops in the forward and dz
+    GEMMs, many 256-column output tiles of d_hidden and d_weight, and a token
+    block cap (32-40 MB of hidden rows) below the token count.  Two-call
+    path and the single call that keeps the logits, against the oracle."""
+    from gpu_helpers import run_gpu_fwd_bwd
+    w = _w(700, H, 1500, 300, 0.9, "bernoulli", mask_drop=0.2, hidden_dist="rms",
+           weight_std=0.01, seed=H)
+    x = W.make_inputs(w)
+    o = run_oracle(x)
+    g = run_gpu(x)
+    assert g["fwd_status"] == 0 and g["bwd_status"] == 0
+    e = assert_parity(g, o)
+    k = run_gpu_fwd_bwd(x, lm.LMHEAD_STRATEGY_KEEP_LOGITS)
+    assert k["status"] == 0
+    ek = assert_parity(k, o)
+    print(H, e, ek)
