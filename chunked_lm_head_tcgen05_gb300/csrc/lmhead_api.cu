@@ -301,6 +301,26 @@ int fwd_m_group(int64_t H) {
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(budget / panel, 1 << 20)));
 }
 
+// Work units of the per-block dz GEMM: k adjacent 256-column tiles of one
+// token block, k the largest of 4, 2, 1 that still leaves at least
+// kDzUnitsPerPair units per CTA pair (so the launch's tail stays short).
+// Each unit pays one fetch from the unit counter and one hand-off through
+// the scheduler ring, which shows where a tile is short (K = H).  Measured on
+// GB300, interleaved, results bitwise equal: dz launches of the 200,000-token
+// trace (H 2048, 40 x 198 tiles per block) 64.7 ms per step with one tile per
+// unit, 62.2 with two, 61.0 with four; a Qwen3-4B-sized block (H 2560,
+// 16 x 66 tiles) 2.04 / 1.96 / 2.10 ms, four tiles leaving too few units.
+constexpr int64_t kDzUnitsPerPair = 6;
+
+int dz_splits(int64_t m_tiles, int64_t n_tiles, int sms) {
+  const int64_t pairs = std::max(1, use_pair() ? sms / 2 : sms);
+  for (int64_t k = 4; k > 1; k /= 2) {
+    const int64_t splits = ceil_div(n_tiles, k);
+    if (m_tiles * splits >= kDzUnitsPerPair * pairs) return static_cast<int>(splits);
+  }
+  return 0;   // one tile per unit
+}
+
 // Single-call forward + backward that keeps each token block's logits over
 // the whole vocabulary (T_b x V_pad 16-bit values <= chunk_size x V) instead
 // of recomputing them.  It pays when the recompute GEMM (2 T H V flops)
@@ -680,6 +700,7 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       pz.dz_out = dz;
       pz.dz_ld = static_cast<int>(bp.Vb);
       pz.out_mode = 1;
+      pz.n_splits = dz_splits(ceil_div(m_cap, um), ceil_div(vact, BN), sms);
       if (!make_map(&lz.map_out[0], dz, vact, m_cap, 2ull * bp.Vb, 64, BM)) return LMHEAD_ERR_CUDA;
       lz.n_problems = 1;
       lz.counter = counter;
