@@ -127,6 +127,19 @@ bool persistent_pays(int64_t Tb, int64_t Vb, int64_t H) {
 int unit_rows() { return use_pair() ? 2 * BM : BM; }
 uint32_t b_box_rows() { return use_pair() ? BN / 2 : BN; }
 
+bool make_map_k3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t row_bytes, uint32_t box_rows);
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+              uint32_t box_inner, uint32_t box_outer);
+
+// Map of a K-major operand with K = H of the forward and dz GEMMs: on CTA
+// pairs those kernels stage two K steps per operand (3-D boxes), single-CTA
+// tiles one (2-D boxes).
+bool make_map_hk(CUtensorMap* m, const void* base, uint64_t H, uint64_t rows, uint32_t box_rows) {
+  return use_pair() ? make_map_k3(m, base, H, rows, 2 * H, box_rows)
+                    : make_map(m, base, H, rows, 2 * H, BK, box_rows);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -181,6 +194,25 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
               uint32_t box_inner, uint32_t box_outer) {
   return make_map_typed(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes,
                         box_inner, box_outer);
+}
+
+// K-major bf16 operand [rows][inner] (inner a multiple of 64: K = H) viewed
+// as (64, rows, inner / 64), the 64-element K chunks 128 bytes apart.  A box
+// of 64 x box_rows x 2 loads two 64-wide K steps with one instruction; each
+// lands as the swizzled image a 2-D 64 x box_rows box would give, 16 KB
+// apart for 128 rows.  Rows past `rows`, and a chunk past the last, read as
+// zero.
+bool make_map_k3(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t row_bytes, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc || inner == 0 || rows == 0 || inner % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, inner / 64};
+  cuuint64_t strides[2] = {row_bytes, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map_f16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
@@ -535,8 +567,8 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
 
   LaunchArgs la;
   std::memset(&la, 0, sizeof(la));
-  if (!make_map(&la.map_a[0], f.h_src, H, f.rows_avail, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-  if (!make_map(&la.map_b[0], weight, H, V, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
+  if (!make_map_hk(&la.map_a[0], f.h_src, H, f.rows_avail, BM)) return LMHEAD_ERR_CUDA;
+  if (!make_map_hk(&la.map_b[0], weight, H, V, b_box_rows())) return LMHEAD_ERR_CUDA;
   GemmArgs& p = la.prob[0].p;
   p.m_cap = static_cast<int>(T);
   p.n_extent = V;
@@ -682,8 +714,8 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
       // dz = cotangent of the recomputed logits of this block, bf16 scratch
       LaunchArgs lz;
       std::memset(&lz, 0, sizeof(lz));
-      if (!make_map(&lz.map_a[0], h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-      if (!make_map(&lz.map_b[0], w_blk, H, vact, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
+      if (!make_map_hk(&lz.map_a[0], h_blk, H, h_rows, BM)) return LMHEAD_ERR_CUDA;
+      if (!make_map_hk(&lz.map_b[0], w_blk, H, vact, b_box_rows())) return LMHEAD_ERR_CUDA;
       GemmArgs& pz = lz.prob[0].p;
       pz.m_cap = static_cast<int>(m_cap);
       pz.n_extent = static_cast<int>(vact);
@@ -846,8 +878,8 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
     // forward over the whole vocabulary for this block, keeping the logits
     LaunchArgs lf;
     std::memset(&lf, 0, sizeof(lf));
-    if (!make_map(&lf.map_a[0], h_blk, H, h_rows, 2ull * H, BK, BM)) return LMHEAD_ERR_CUDA;
-    if (!make_map(&lf.map_b[0], weight, H, V, 2ull * H, BK, b_box_rows())) return LMHEAD_ERR_CUDA;
+    if (!make_map_hk(&lf.map_a[0], h_blk, H, h_rows, BM)) return LMHEAD_ERR_CUDA;
+    if (!make_map_hk(&lf.map_b[0], weight, H, V, b_box_rows())) return LMHEAD_ERR_CUDA;
     if (!make_map_f16(&lf.map_out[0], zbuf, V, m_cap, 2ull * fp.V_pad, 64, BM))
       return LMHEAD_ERR_CUDA;
     GemmArgs& pf = lf.prob[0].p;

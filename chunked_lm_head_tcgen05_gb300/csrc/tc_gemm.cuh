@@ -19,7 +19,9 @@
 // half (128 columns) of B, the even CTA issues tcgen05.mma.cta_group::2
 // (M = 256) over both CTAs' shared memory, and each CTA's TMEM receives its
 // 128 rows of D.  Per SM this halves the B traffic and the B staging space,
-// so six stages fit instead of four.  The even CTA fetches the work units and
+// so six 64-wide K steps fit instead of four.  Where both operands are
+// K-major with K = H (forward and dz tiles), a pair stages them two K steps
+// at a time (three 64 KB stages, one 3-D TMA box per operand each).  The even CTA fetches the work units and
 // forwards them to its peer; the peer's loads complete on the even CTA's
 // barriers, and MMA completion is multicast back to both CTAs.
 //
@@ -205,6 +207,17 @@ template <int EPI, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ LaunchArgs L) {
   using C = TileCfg<PAIR>;
+  // K steps per operand stage.  Where both operands are K-major with K = H
+  // (the forward kernels and the per-block dz GEMM) and the tile is a CTA
+  // pair's, a stage holds two 64-wide K steps of each operand, loaded by one
+  // 3-D TMA box per operand (64 elements x rows x 2 K chunks): half the TMA
+  // instructions and barrier round trips per K step.  The host passes
+  // K-major 3-D maps (make_map_k3) and never an MN-major A for these.
+  constexpr int KS = (PAIR && !B_MN && EPI != EPI_STORE_F32) ? 2 : 1;
+  constexpr int NST = C::NSTAGE / KS;
+  constexpr uint32_t STG = C::STAGE * KS;
+  constexpr uint32_t ABYTES = A_TILE_BYTES * KS;
+  static_assert(NST * KS == C::NSTAGE, "stage ring does not divide into K-step pairs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NSTAGE; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), 1);
     }
@@ -331,20 +344,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const int arow = m * C::UNIT_M + static_cast<int>(rank) * BM;
           for (int n = nb; ok && n < ne; ++n) {
             const int bcol = n * BN + static_cast<int>(rank) * C::B_ROWS;
-            for (int kb = 0; kb < s.k_blocks; ++kb) {
-              if (leader && ahead < 0 && n == ne - 1 && kb == max(0, s.k_blocks - FETCH_AHEAD_KB))
+            const int kb_fetch = (max(0, s.k_blocks - FETCH_AHEAD_KB) / KS) * KS;
+            for (int kb = 0; kb < s.k_blocks; kb += KS) {
+              if (leader && ahead < 0 && n == ne - 1 && kb == kb_fetch)
                 ahead = atomicAdd(L.counter, 1);
               if (!wait_bounded<PAIR>(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, status)) {
                 ok = false;
                 break;
               }
               const uint32_t fb_local = smem_addr(&ctl->full[stage]);
-              if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * C::CTAS);
-              const uint32_t sa = smem_base + stage * C::STAGE;
-              const uint32_t sb = sa + A_TILE_BYTES;
+              if (leader) mbar_arrive_expect_tx(fb_local, STG * C::CTAS);
+              const uint32_t sa = smem_base + stage * STG;
+              const uint32_t sb = sa + ABYTES;
               // MN-major operands use 3-D maps (64 elements, K rows, 64-element
               // chunks): one instruction loads all of this CTA's chunks
-              if constexpr (PAIR) {
+              if constexpr (KS == 2) {
+                // K chunks kb and kb + 1 of the K-major 3-D maps land 16 KB
+                // apart, each the swizzled image of one 64-wide K step; past
+                // the last chunk the box reads zeros (never multiplied)
+                const uint32_t fb = map_to_cta(fb_local, 0);
+                tma_load_3d_pair(sa, ma, fb, 0, arow, kb);
+                tma_load_3d_pair(sb, mb, fb, 0, bcol, kb);
+              } else if constexpr (PAIR) {
                 const uint32_t fb = map_to_cta(fb_local, 0);
                 if constexpr (!A_MN)
                   tma_load_2d_pair(sa, ma, fb, kb * BK, arow);
@@ -366,14 +387,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
               issued_mask |= 1u << stage;
               issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
-              if (++stage == C::NSTAGE) {
+              if (++stage == NST) {
                 stage = 0;
                 phase ^= 1;
               }
             }
           }
         };
-        if (L.prob[q].a_mn != 0)
+        if (KS == 1 && L.prob[q].a_mn != 0)
           produce(std::true_type{});
         else
           produce(std::false_type{});
@@ -382,7 +403,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if constexpr (PAIR) {
           pause_ns(100000);   // let copies already issued land before exit
         } else {
-          for (int s = 0; s < C::NSTAGE; ++s)
+          for (int s = 0; s < NST; ++s)
             if (issued_mask & (1u << s))
               wait_drain(smem_addr(&ctl->full[s]), (issued_par >> s) & 1);
         }
@@ -420,33 +441,40 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + acc * BN;
-            for (int kb = 0; kb < s.k_blocks; ++kb) {
+            for (int kb = 0; kb < s.k_blocks; kb += KS) {
               if (!wait_bounded<PAIR>(smem_addr(&ctl->full[stage]), phase, abort, status)) {
                 ok = false;
                 break;
               }
               tc_fence_after_sync();
-              const uint32_t sa = smem_base + stage * C::STAGE;
-              const uint32_t sb = sa + A_TILE_BYTES;
+              const uint32_t sa0 = smem_base + stage * STG;
+              const uint32_t sb0 = sa0 + ABYTES;
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                // K-major: the next 16 K elements are 32 bytes further along the
-                // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further,
-                // with the 64-wide MN chunks 8 KB apart.
-                const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                         : smem_desc_sw128(sa + k * 32, 16, 1024);
-                const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, B_LBO, 1024)
-                                         : smem_desc_sw128(sb + k * 32, 16, 1024);
-                if constexpr (PAIR)
-                  umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
-                else
-                  umma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+              for (int j = 0; j < KS; ++j) {
+                if (kb + j >= s.k_blocks) break;   // zero-filled K step past the end
+                const uint32_t sa = sa0 + j * A_TILE_BYTES;
+                const uint32_t sb = sb0 + j * C::B_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                  // K-major: the next 16 K elements are 32 bytes further along the
+                  // swizzled 128-byte row.  MN-major: 16 more K rows, 2 KB further,
+                  // with the 64-wide MN chunks 8 KB apart.
+                  const uint64_t ad = A_MN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                           : smem_desc_sw128(sa + k * 32, 16, 1024);
+                  const uint64_t bd = B_MN ? smem_desc_sw128(sb + k * 2048, B_LBO, 1024)
+                                           : smem_desc_sw128(sb + k * 32, 16, 1024);
+                  const uint32_t accum = (kb | j | k) != 0 ? 1u : 0u;
+                  if constexpr (PAIR)
+                    umma_bf16_pair(d_tmem, ad, bd, IDESC, accum);
+                  else
+                    umma_bf16(d_tmem, ad, bd, IDESC, accum);
+                }
               }
               if constexpr (PAIR)
                 umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
               else
                 umma_commit(smem_addr(&ctl->empty[stage]));
-              if (++stage == C::NSTAGE) {
+              if (++stage == NST) {
                 stage = 0;
                 phase ^= 1;
               }
@@ -460,7 +488,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (acc == 0) acc_phase ^= 1;
           }
         };
-        if (L.prob[q].a_mn != 0)
+        if (KS == 1 && L.prob[q].a_mn != 0)
           issue(std::true_type{});
         else
           issue(std::false_type{});
