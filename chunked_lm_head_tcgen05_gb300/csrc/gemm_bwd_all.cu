@@ -177,16 +177,6 @@ __device__ __forceinline__ bool wait_flag(const int* f, int target, volatile int
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bwd_all_kernel(const __grid_constant__ BwdAllArgs A) {
   using C = TileCfg<true>;
-  // Every tile kind stages two 64-wide K steps per operand, each operand
-  // loaded by one 3-D TMA box (64 elements x 128 rows x 2 chunks): dz tiles
-  // read K-major hidden and W chunks; dh tiles read the dz scratch K-major
-  // through its chunked view and W MN-major; dW tiles read dz and hidden
-  // MN-major, 128 K rows per box.
-  constexpr int KS = 2;
-  constexpr int NST = C::NSTAGE / KS;
-  constexpr uint32_t STG = C::STAGE * KS;
-  constexpr uint32_t ABYTES = A_TILE_BYTES * KS;
-  static_assert(NST * KS == C::NSTAGE, "stage ring does not divide into K-step pairs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -204,7 +194,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), 1);
     }
@@ -336,8 +326,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // this TMA-issue-bound thread about a tenth of the kernel's speed.
         auto produce = [&](auto kind_tag) {
           constexpr int KIND = decltype(kind_tag)::value;
-          const int kb_fetch = (max(0, x.kblocks - FETCH_AHEAD_KB) / KS) * KS;
-          for (int kb = 0; kb < x.kblocks; kb += KS) {
+          for (int kb = 0; kb < x.kblocks; ++kb) {
             if constexpr (KIND == U_DH) {
               if (!dz_ready && kb % (BN / BK) == 0) {
                 if (ld_acquire_gpu(F.dz_all(x.b)) >= dz_target) {
@@ -349,33 +338,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 fence_async_global();
               }
             }
-            if (leader && ahead < 0 && kb == kb_fetch)
+            if (leader && ahead < 0 && kb == max(0, x.kblocks - FETCH_AHEAD_KB))
               ahead = atomicAdd(A.unit_counter, 1);
             if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, st)) {
               ok = false;
               break;
             }
             const uint32_t fb_local = smem_addr(&ctl->full[stage]);
-            if (leader) mbar_arrive_expect_tx(fb_local, STG * 2);
+            if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * 2);
             const uint32_t fb = map_to_cta(fb_local, 0);
-            const uint32_t sa = smem_base + stage * STG;
-            const uint32_t sb = sa + ABYTES;
+            const uint32_t sa = smem_base + stage * C::STAGE;
+            const uint32_t sb = sa + A_TILE_BYTES;
             const int k0 = kb * BK;
-            // K steps kb and kb + 1.  Past a K extent that is an odd number of
-            // steps the second is either zero-filled or dz this block already
-            // stored (its dz tiles cover whole 256-column, 256-row tiles);
-            // the MMA warp skips it.
             if constexpr (KIND == U_DZ) {
-              tma_load_3d_pair(sa, &A.h_k, fb, 0, x.k.t0 + mrow, kb);
-              tma_load_3d_pair(sb, &A.w_k, fb, 0, x.k.v0 + ncol, kb);
+              tma_load_2d_pair(sa, &A.h_k, fb, k0, x.k.t0 + mrow);
+              tma_load_2d_pair(sb, &A.w_k, fb, k0, x.k.v0 + ncol);
             } else if constexpr (KIND == U_DH) {
-              tma_load_3d_pair(sa, &A.dz_mn, fb, 0, mrow, kb);
+              tma_load_2d_pair(sa, &A.dz_k, fb, k0, mrow);
               tma_load_3d_pair(sb, &A.w_mn, fb, 0, x.k.v0 + k0, ncol / 64);
             } else {
               tma_load_3d_pair(sa, &A.dz_mn, fb, 0, k0, mrow / 64);
               tma_load_3d_pair(sb, &A.h_mn, fb, 0, x.k.t0 + k0, ncol / 64);
             }
-            if (++stage == NST) {
+            if (++stage == C::NSTAGE) {
               stage = 0;
               phase ^= 1;
             }
@@ -418,34 +403,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           constexpr int KIND = decltype(kind_tag)::value;
           constexpr bool AMN = KIND == U_DW, BMN = KIND != U_DZ;
           constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, AMN, BMN);
-          for (int kb = 0; kb < x.kblocks; kb += KS) {
+          for (int kb = 0; kb < x.kblocks; ++kb) {
             if (!wait_bar(smem_addr(&ctl->full[stage]), phase, abort, st)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
-            const uint32_t sa0 = smem_base + stage * STG;
-            const uint32_t sb0 = sa0 + ABYTES;
+            const uint32_t sa = smem_base + stage * C::STAGE;
+            const uint32_t sb = sa + A_TILE_BYTES;
 #pragma unroll
-            for (int j = 0; j < KS; ++j) {
-              if (kb + j >= x.kblocks) break;   // the second K step is past the end
-              // K-major: each K step is a 16 KB image (128 rows x 128 bytes) and
-              // 16 more K elements are 32 bytes along the swizzled row.
-              // MN-major: each 64-wide MN chunk holds 128 K rows (16 KB), so a K
-              // step is 8 KB further and 16 more K rows 2 KB further.
-              const uint32_t sa = sa0 + j * (AMN ? 8192u : 16384u);
-              const uint32_t sb = sb0 + j * (BMN ? 8192u : 16384u);
-#pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                const uint64_t ad = AMN ? smem_desc_sw128(sa + k * 2048, 16384, 1024)
-                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
-                const uint64_t bd = BMN ? smem_desc_sw128(sb + k * 2048, 16384, 1024)
-                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
-                umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | j | k) != 0 ? 1u : 0u);
-              }
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: 16 more K elements are 32 bytes along the swizzled row;
+              // MN-major: 16 more K rows are 2 KB further, 64-wide MN chunks 8 KB apart.
+              const uint64_t ad = AMN ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
+              const uint64_t bd = BMN ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
             }
             umma_commit_pair(smem_addr(&ctl->empty[stage]), 0x3);
-            if (++stage == NST) {
+            if (++stage == C::NSTAGE) {
               stage = 0;
               phase ^= 1;
             }

@@ -118,15 +118,12 @@ struct LaunchArgs {
 constexpr int BWD_ALL_MAX_TOKEN_BLOCKS = 255;
 
 struct BwdAllArgs {
-  // Operand maps: every box is 64 x 128 x 2 and stages two 64-wide K steps.
-  CUtensorMap h_k;     // hidden rows as (64, rows, H / 64 chunks): K-major A of dz
-  CUtensorMap w_k;     // W as (64, V rows, H / 64 chunks): K-major B of dz (half of N per CTA)
-  CUtensorMap dz_k;    // dz scratch [T_b, V_b], 2-D boxes 64 x 128: dz tile stores
-  CUtensorMap w_mn;    // W as (64, V rows, H / 64 chunks): MN-major B of dh (128 K rows)
-  CUtensorMap dz_mn;   // dz scratch as (64, T_b rows, V_b / 64 chunks): K-major A of dh
-                       // (128 token rows x 2 vocabulary chunks) and MN-major A of dW
-                       // (128 K rows = tokens x 2 vocabulary chunks)
-  CUtensorMap h_mn;    // hidden rows as (64, rows, H / 64 chunks): MN-major B of dW (128 K rows)
+  CUtensorMap h_k;     // hidden rows [rows, H], K-major, boxes 64 x 128: A of dz
+  CUtensorMap w_k;     // W [V, H], K-major, boxes 64 x 128: B of dz (half of N per CTA)
+  CUtensorMap dz_k;    // dz scratch [T_b, V_b], boxes 64 x 128: dz tile stores and A of dh
+  CUtensorMap w_mn;    // W as (64, V rows, H / 64 chunks), boxes 64 x 64 x 2: MN-major B of dh
+  CUtensorMap dz_mn;   // dz scratch as (64, T_b rows, V_b / 64 chunks), boxes 64 x 64 x 2: A of dW
+  CUtensorMap h_mn;    // hidden rows as (64, rows, H / 64 chunks), boxes 64 x 64 x 2: B of dW
   CUtensorMap dh_out;  // d_hidden fp32 [T, H], boxes 32 x 128 (when rows are not scattered)
   CUtensorMap dw_out;  // d_weight fp32 [V, H], boxes 32 x 128
   int T_b, V_b, n_tb, n_vb, V, H, T_alloc;

@@ -178,12 +178,12 @@ bool make_map_typed(CUtensorMap* m, CUtensorMapDataType type, const void* base, 
 // zero; a partial last chunk reads the row's padding (callers discard those
 // M rows, or the row is padded with zeros).
 bool make_map_mn(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
-                 uint64_t row_bytes, uint32_t chunks, uint32_t k_rows = 64) {
+                 uint64_t row_bytes, uint32_t chunks) {
   auto enc = encode_fn();
   if (!enc || inner == 0 || rows == 0) return false;
   cuuint64_t dims[3] = {64, rows, (inner + 63) / 64};
   cuuint64_t strides[2] = {row_bytes, 128};
-  cuuint32_t box[3] = {64, k_rows, chunks};
+  cuuint32_t box[3] = {64, 64, chunks};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -656,13 +656,12 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
     BwdAllArgs a;
     std::memset(&a, 0, sizeof(a));
     const uint64_t Tb = static_cast<uint64_t>(bp.Tb), Vb = static_cast<uint64_t>(bp.Vb);
-    // operand boxes of 128 rows x 2 chunks: two K steps per stage
-    if (!make_map_k3(&a.h_k, f.h_src, H, f.rows_avail, 2ull * H, BM) ||
-        !make_map_k3(&a.w_k, weight, H, V, 2ull * H, BN / 2) ||
+    if (!make_map(&a.h_k, f.h_src, H, f.rows_avail, 2ull * H, BK, BM) ||
+        !make_map(&a.w_k, weight, H, V, 2ull * H, BK, BN / 2) ||
         !make_map(&a.dz_k, dz, Vb, Tb, 2ull * Vb, 64, BM) ||
-        !make_map_mn(&a.w_mn, weight, H, V, 2ull * H, 2, 128) ||
-        !make_map_mn(&a.dz_mn, dz, Vb, Tb, 2ull * Vb, 2, 128) ||
-        !make_map_mn(&a.h_mn, f.h_src, H, f.rows_avail, 2ull * H, 2, 128) ||
+        !make_map_mn(&a.w_mn, weight, H, V, 2ull * H, 2) ||
+        !make_map_mn(&a.dz_mn, dz, Vb, Tb, 2ull * Vb, 2) ||
+        !make_map_mn(&a.h_mn, f.h_src, H, f.rows_avail, 2ull * H, 2) ||
         (!f.idx && !make_out_map_f32(&a.dh_out, d_hidden, H, T, H)) ||
         !make_out_map_f32(&a.dw_out, d_weight, H, V, H))
       return LMHEAD_ERR_CUDA;
