@@ -28,8 +28,9 @@
 // A launch holds one or two problems (see LaunchArgs).  A work unit is one
 // block of M rows (128, or 256 for a pair) and a contiguous range of
 // 256-column N tiles: for the forward statistics the range is a vocabulary
-// split (the running softmax statistics stay in registers across it);
-// otherwise a unit is one tile.  Units of problem 0 are numbered first.
+// split (the running softmax statistics stay in registers across it); for
+// the per-block dz GEMM a few adjacent tiles (the host sets n_splits);
+// otherwise one tile.  Units of problem 0 are numbered first.
 // Fetching units dynamically keeps every SM busy until the end when units
 // differ in length or speed.  Every unit is computed entirely by one CTA (or
 // pair) in a fixed order, so results do not depend on who took it.
