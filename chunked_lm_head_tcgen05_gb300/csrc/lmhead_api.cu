@@ -326,8 +326,9 @@ constexpr int64_t kFwdGroupBytes = 32ll << 20;
 int fwd_m_group(int64_t H) {
   int64_t budget = kFwdGroupBytes;
   if (const char* e = std::getenv("LMHEAD_FWD_GROUP_MB"); e && e[0]) {
-    budget = std::atoll(e) << 20;
-    if (budget <= 0) return 0;
+    const long long mb = std::atoll(e);
+    if (mb <= 0) return 0;
+    budget = static_cast<int64_t>(std::min<long long>(mb, 1ll << 20)) << 20;
   }
   const int64_t panel = static_cast<int64_t>(unit_rows()) * 2 * H;
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(budget / panel, 1 << 20)));
