@@ -205,6 +205,40 @@ class OracleSample:
                 "rows), %.2f s per pass" % (n, self.w.name, self.w.V, dt))
 
 
+def cublas_same_shape(h, w, stream, reps):
+    """Plain bf16 GEMMs (torch.matmul, i.e. cuBLAS; bf16 in and out) of the head's three
+    contraction shapes with the [T, V] logits materialised: logits = h W^T,
+    d_hidden = dz W, d_weight = dz^T h.  Context for the fused kernels, which never
+    hold [T, V] and add their epilogues; not a path of the head."""
+    import torch
+    T, H = h.shape
+    V = w.shape[0]
+    gen = torch.Generator(device=h.device).manual_seed(7)
+    dz = torch.randn((T, V), device=h.device, dtype=torch.bfloat16, generator=gen)
+    z = torch.empty((T, V), device=h.device, dtype=torch.bfloat16)
+    dh = torch.empty((T, H), device=h.device, dtype=torch.bfloat16)
+    dw = torch.empty((V, H), device=h.device, dtype=torch.bfloat16)
+    ops = {"logits": lambda: torch.matmul(h, w.t(), out=z),
+           "d_hidden": lambda: torch.matmul(dz, w, out=dh),
+           "d_weight": lambda: torch.matmul(dz.t(), h, out=dw)}
+    flops = 2.0 * T * H * V
+    res = {}
+    for name, fn in ops.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12}
+    del dz, z, dh, dw
+    return res
+
+
 def cpu_model():
     """Host CPU description (model name, or the architecture where /proc has none)."""
     import platform
@@ -496,6 +530,19 @@ def run_ours(args, rank, world, local):
               "logits_bytes_bf16": 2 * T * V,
               "workspace_over_logits": ws.numel() / (2.0 * T * V)}
 
+    # ---- context: the same contractions as plain cuBLAS GEMMs (logits materialised)
+    cublas = None
+    if 2 * T * V <= (4 << 30):
+        cublas = cublas_same_shape(g["hidden"], g["weight"], stream, nb)
+        fk = kernels.get("fwd_stats_gemm")
+        cublas["fused_fwd_stats_gemm_tflops"] = (2.0 * Tv * H * V / (fk["ms_per_step"] / 1e3) / 1e12
+                                                 if fk else None)
+        cublas["fused_dominant_kernel"] = {"kernel": roofline["kernel"],
+                                           "tflops_executed": roofline["achieved"]}
+        cublas["note"] = ("torch.matmul bf16 in / bf16 out on the head's three shapes, [T, V] "
+                          "materialised, timed alone; the fused kernels add their epilogues and "
+                          "never hold [T, V]")
+
     counted = 6.0 * Tv * H * V
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -520,6 +567,7 @@ def run_ours(args, rank, world, local):
         "breakdown": breakdown,
         "graph_replay": graph_replay,
         "memory": memory,
+        "cublas_same_shape": cublas,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
