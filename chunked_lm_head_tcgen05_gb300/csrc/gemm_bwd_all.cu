@@ -61,13 +61,20 @@ __device__ __forceinline__ Blk block_of(const BwdAllArgs& a, int tb, int vb, int
   return k;
 }
 
+// A dz unit covers DZW adjacent 256-column tiles of one row tile (the last
+// of a block's columns may be alone): each unit pays a fetch from the unit
+// counter, a scheduler hand-off and a decode, and dz tiles are short (K = H).
+constexpr int DZW = 2;
+
+__device__ __forceinline__ int dz_units(int mt, int nt) { return mt * ((nt + DZW - 1) / DZW); }
+
 // Work units of one full-width block whose token block has `mt` row tiles.
 __device__ __forceinline__ int units_full(const BwdAllArgs& a, int mt, int ht) {
-  return mt * a.NT + mt * ht + a.NT * ht;
+  return dz_units(mt, a.NT) + mt * ht + a.NT * ht;
 }
 
 struct Unit {
-  int kind, b, m, n, kblocks;
+  int kind, b, m, n, ntiles, kblocks;   // dz units: tiles n .. n + ntiles - 1; others: 1 tile
   Blk k;
 };
 
@@ -92,11 +99,15 @@ __device__ __forceinline__ Unit decode(const BwdAllArgs& a, const int* tb_prefix
   Unit x;
   x.k = block_of(a, lo, vb, scored);
   x.b = lo * a.n_vb + vb;
-  const int n_dz = x.k.mt * x.k.nt, n_dh = x.k.mt * ht;
+  const int n_dz = dz_units(x.k.mt, x.k.nt), n_dh = x.k.mt * ht;
+  x.ntiles = 1;
   if (r < n_dz) {
+    // column pairs, row tiles fastest: a block's dz columns complete in order
     x.kind = U_DZ;
-    x.n = r / x.k.mt;
-    x.m = r - x.n * x.k.mt;
+    const int np = r / x.k.mt;
+    x.m = r - np * x.k.mt;
+    x.n = np * DZW;
+    x.ntiles = min(DZW, x.k.nt - x.n);
     x.kblocks = a.H / BK;
   } else if (r - n_dz < n_dh) {
     r -= n_dz;
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const Blk k = block_of(A, tb, 0, scored);
       acc += (A.n_vb - 1) * units_full(A, k.mt, ht);
       const Blk kl = block_of(A, tb, A.n_vb - 1, scored);
-      acc += kl.mt * kl.nt + kl.mt * ht + kl.nt * ht;
+      acc += dz_units(kl.mt, kl.nt) + kl.mt * ht + kl.nt * ht;
     }
     tb_prefix[A.n_tb] = acc;
   }
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int tb = b / A.n_vb, vb = b - tb * A.n_vb;
       const Blk k0 = block_of(A, tb, 0, scored);
       const Blk k = block_of(A, tb, vb, scored);
-      return tb_prefix[tb] + vb * units_full(A, k0.mt, ht) + k.mt * k.nt;
+      return tb_prefix[tb] + vb * units_full(A, k0.mt, ht) + dz_units(k.mt, k.nt);
     };
     if (A.window > 0) unit_begin = first_dh(A.window - 1);
     if (A.window < n_blocks) unit_end = first_dh(A.window);
@@ -326,43 +337,48 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         // this TMA-issue-bound thread about a tenth of the kernel's speed.
         auto produce = [&](auto kind_tag) {
           constexpr int KIND = decltype(kind_tag)::value;
-          for (int kb = 0; kb < x.kblocks; ++kb) {
-            if constexpr (KIND == U_DH) {
-              if (!dz_ready && kb % (BN / BK) == 0) {
-                if (ld_acquire_gpu(F.dz_all(x.b)) >= dz_target) {
-                  dz_ready = true;
-                } else if (!wait_flag(F.dz_col(x.b, kb / (BN / BK)), 2 * x.k.mt, abort, st)) {
-                  ok = false;
-                  break;
+          const int ntl = KIND == U_DZ ? x.ntiles : 1;
+          for (int t = 0; ok && t < ntl; ++t) {
+            const int ncol_t = ncol + t * BN;
+            const bool last_tile = t == ntl - 1;
+            for (int kb = 0; kb < x.kblocks; ++kb) {
+              if constexpr (KIND == U_DH) {
+                if (!dz_ready && kb % (BN / BK) == 0) {
+                  if (ld_acquire_gpu(F.dz_all(x.b)) >= dz_target) {
+                    dz_ready = true;
+                  } else if (!wait_flag(F.dz_col(x.b, kb / (BN / BK)), 2 * x.k.mt, abort, st)) {
+                    ok = false;
+                    break;
+                  }
+                  fence_async_global();
                 }
-                fence_async_global();
               }
-            }
-            if (leader && ahead < 0 && kb == max(0, x.kblocks - FETCH_AHEAD_KB))
-              ahead = atomicAdd(A.unit_counter, 1);
-            if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, st)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb_local = smem_addr(&ctl->full[stage]);
-            if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * 2);
-            const uint32_t fb = map_to_cta(fb_local, 0);
-            const uint32_t sa = smem_base + stage * C::STAGE;
-            const uint32_t sb = sa + A_TILE_BYTES;
-            const int k0 = kb * BK;
-            if constexpr (KIND == U_DZ) {
-              tma_load_2d_pair(sa, &A.h_k, fb, k0, x.k.t0 + mrow);
-              tma_load_2d_pair(sb, &A.w_k, fb, k0, x.k.v0 + ncol);
-            } else if constexpr (KIND == U_DH) {
-              tma_load_2d_pair(sa, &A.dz_k, fb, k0, mrow);
-              tma_load_3d_pair(sb, &A.w_mn, fb, 0, x.k.v0 + k0, ncol / 64);
-            } else {
-              tma_load_3d_pair(sa, &A.dz_mn, fb, 0, k0, mrow / 64);
-              tma_load_3d_pair(sb, &A.h_mn, fb, 0, x.k.t0 + k0, ncol / 64);
-            }
-            if (++stage == C::NSTAGE) {
-              stage = 0;
-              phase ^= 1;
+              if (leader && ahead < 0 && last_tile && kb == max(0, x.kblocks - FETCH_AHEAD_KB))
+                ahead = atomicAdd(A.unit_counter, 1);
+              if (!wait_bar(smem_addr(&ctl->empty[stage]), phase ^ 1, abort, st)) {
+                ok = false;
+                break;
+              }
+              const uint32_t fb_local = smem_addr(&ctl->full[stage]);
+              if (leader) mbar_arrive_expect_tx(fb_local, C::STAGE * 2);
+              const uint32_t fb = map_to_cta(fb_local, 0);
+              const uint32_t sa = smem_base + stage * C::STAGE;
+              const uint32_t sb = sa + A_TILE_BYTES;
+              const int k0 = kb * BK;
+              if constexpr (KIND == U_DZ) {
+                tma_load_2d_pair(sa, &A.h_k, fb, k0, x.k.t0 + mrow);
+                tma_load_2d_pair(sb, &A.w_k, fb, k0, x.k.v0 + ncol_t);
+              } else if constexpr (KIND == U_DH) {
+                tma_load_2d_pair(sa, &A.dz_k, fb, k0, mrow);
+                tma_load_3d_pair(sb, &A.w_mn, fb, 0, x.k.v0 + k0, ncol_t / 64);
+              } else {
+                tma_load_3d_pair(sa, &A.dz_mn, fb, 0, k0, mrow / 64);
+                tma_load_3d_pair(sb, &A.h_mn, fb, 0, x.k.t0 + k0, ncol_t / 64);
+              }
+              if (++stage == C::NSTAGE) {
+                stage = 0;
+                phase ^= 1;
+              }
             }
           }
         };
@@ -392,12 +408,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (u < 0) break;
         const Unit x = decode(A, tb_prefix, scored, ht, u);
         if (x.kblocks == 0) continue;
-        if (!wait_bar(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, st)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + acc * BN;
+        uint32_t d_tmem = 0;
         // one K loop per tile kind, operand layouts and descriptor fixed at compile time
         auto issue = [&](auto kind_tag) {
           constexpr int KIND = decltype(kind_tag)::value;
@@ -428,16 +439,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         };
-        if (x.kind == U_DZ)
-          issue(std::integral_constant<int, U_DZ>{});
-        else if (x.kind == U_DH)
-          issue(std::integral_constant<int, U_DH>{});
-        else
-          issue(std::integral_constant<int, U_DW>{});
+        // each tile of the unit into the next free accumulator
+        for (int t = 0; t < x.ntiles; ++t) {
+          if (!wait_bar(smem_addr(&ctl->tempty[acc]), acc_phase ^ 1, abort, st)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          d_tmem = tmem_base + acc * BN;
+          if (x.kind == U_DZ)
+            issue(std::integral_constant<int, U_DZ>{});
+          else if (x.kind == U_DH)
+            issue(std::integral_constant<int, U_DH>{});
+          else
+            issue(std::integral_constant<int, U_DW>{});
+          if (!ok) break;
+          umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
         if (!ok) break;
-        umma_commit_pair(smem_addr(&ctl->tfull[acc]), 0x3);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
       }
       // every MMA issued by this thread has completed before TMEM is freed
       umma_commit_pair(smem_addr(&ctl->drain), 0x1);
@@ -509,10 +530,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (u < 0) break;
       const Unit x = decode(A, tb_prefix, scored, ht, u);
       const int rloc = x.m * PAIR_M + r128 + lrow;   // this thread's row within the block's tile grid
-      const int col0 = x.n * BN;
 
       if (x.kblocks == 0) {
         // a dW tile of a token block without scored tokens: zeros unless it adds
+        const int col0 = x.n * BN;
         if (x.k.tb == 0 && !A.accumulate_dweight && rloc < x.k.vact) {
           float* dst = A.d_weight + static_cast<int64_t>(x.k.v0 + rloc) * A.H + col0;
           const int lim = min(BN, A.H - col0);
@@ -522,138 +543,152 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         continue;
       }
 
-      // dependencies of this tile's stores
-      bool dep_ok = true;
-      if (x.kind == U_DZ) {
-        if (x.b > 0) {
-          const Blk kp = block_of(A, (x.b - 1) / A.n_vb, (x.b - 1) % A.n_vb, scored);
-          const int bp = x.n < kp.nt ? x.b - 1 : x.b - 2;
-          dep_ok = wait_deps(F.dh_row(x.b - 1, x.m), 2 * ht, bp >= 0 ? F.dw_col(bp, x.n) : nullptr,
-                             2 * ht);
-        }
-      } else if (x.kind == U_DH) {
-        if (x.k.vb > 0) dep_ok = wait_deps(F.dh_row(x.b - 1, x.m), 2 * ht, nullptr, 0);
-      } else {
-        if (x.k.tb > 0) dep_ok = wait_deps(F.dw_col(x.b - A.n_vb, x.m), 2 * ht, nullptr, 0);
-      }
-      if (!dep_ok) break;
-
-      int t_ok = 0;
-      if (issuer) t_ok = wait_bar(smem_addr(&ctl->tfull[acc]), acc_phase, abort, st) ? 1 : 0;
-      if (!broadcast(t_ok)) break;
-      tc_fence_after_sync();
-      const uint32_t tcol = tmem_base + lane_off + acc * BN;
-      auto release_acc = [&]() {
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tempty_leader + acc * sizeof(uint64_t));
-      };
-
-      if (x.kind == U_DZ) {
-        const bool row_ok = rloc < x.k.mcap;
-        float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
-        int y = -1;
-        if (row_ok) {
-          cf = A.coef[x.k.t0 + rloc];
-          y = A.y_c[x.k.t0 + rloc];
-        }
-        const int yt = y - x.k.v0 - col0;
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 64; ++cc) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float v[32];
-            tmem_load_32(tcol + cc * 64 + h * 32, v);
-            if (cc == BN / 64 - 1 && h == 1) release_acc();
-            const int cb = cc * 64 + h * 32;
-            float g[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float d = fmaf(v[j], A.scale, -cf.x);
-              const float pr = ex2_approx(d);
-              g[j] = -pr * fmaf(cf.y, d, cf.z);
-            }
-            if (static_cast<unsigned>(yt - cb) < 32u) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j == yt - cb) g[j] += cf.w;
-            }
-            // columns past the vocabulary block hold zeros: the dh and dW
-            // tiles read whole 64-wide K steps of the scratch
-            const int lim = x.k.vact - col0 - cb;
-            if (lim < 32) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j >= lim) g[j] = 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
+      // the unit's tiles in order (dz units may hold two), each from the next
+      // accumulator the MMA warp filled
+      bool fail = false;
+      for (int t = 0; t < x.ntiles; ++t) {
+        const int xn = x.n + t;
+        const int col0 = xn * BN;
+        // dependencies of this tile's stores
+        bool dep_ok = true;
+        if (x.kind == U_DZ) {
+          if (x.b > 0) {
+            const Blk kp = block_of(A, (x.b - 1) / A.n_vb, (x.b - 1) % A.n_vb, scored);
+            const int bp = xn < kp.nt ? x.b - 1 : x.b - 2;
+            dep_ok = wait_deps(F.dh_row(x.b - 1, x.m), 2 * ht, bp >= 0 ? F.dw_col(bp, xn) : nullptr,
+                               2 * ht);
           }
-          stage_out(pk, stg0, nstore++, lrow, issuer, &A.dz_k, 1, col0 + cc * 64,
-                    x.m * PAIR_M + r128, &st->status);
+        } else if (x.kind == U_DH) {
+          if (x.k.vb > 0) dep_ok = wait_deps(F.dh_row(x.b - 1, x.m), 2 * ht, nullptr, 0);
+        } else {
+          if (x.k.tb > 0) dep_ok = wait_deps(F.dw_col(x.b - A.n_vb, x.m), 2 * ht, nullptr, 0);
         }
-        signal(F.dz_col(x.b, x.n), F.dz_all(x.b), true);
-      } else if (x.kind == U_DH) {
-        const bool scatter = A.row_map != nullptr;
-        const bool add = x.k.vb > 0;
-        const bool row_ok = rloc < x.k.rows;
-        const int64_t orow = (scatter && row_ok) ? A.row_map[x.k.t0 + rloc] : 0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_load_32(tcol + c * 32, v);
-          if (c == BN / 32 - 1) release_acc();
-          const int cb = c * 32;
-          if (!scatter) {
-            uint32_t w[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
-            stage_out(w, stg0, nstore++, lrow, issuer, &A.dh_out, add ? 2 : 1, col0 + cb,
-                      x.k.t0 + x.m * PAIR_M + r128, &st->status);
-          } else if (row_ok) {
-            const int lim = A.H - col0 - cb;
-            float* dst = A.d_hidden + orow * A.H + col0 + cb;
-            if (lim >= 32) {
-              float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-                if (add) {
-                  // from L2: the previous value was written by another SM
-                  const float4 old = __ldcg(d4 + k);
-                  o.x += old.x;
-                  o.y += old.y;
-                  o.z += old.z;
-                  o.w += old.w;
-                }
-                d4[k] = o;
+        if (!dep_ok) {
+          fail = true;
+          break;
+        }
+
+        int t_ok = 0;
+        if (issuer) t_ok = wait_bar(smem_addr(&ctl->tfull[acc]), acc_phase, abort, st) ? 1 : 0;
+        if (!broadcast(t_ok)) {
+          fail = true;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t tcol = tmem_base + lane_off + acc * BN;
+        auto release_acc = [&]() {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(tempty_leader + acc * sizeof(uint64_t));
+        };
+
+        if (x.kind == U_DZ) {
+          const bool row_ok = rloc < x.k.mcap;
+          float4 cf = make_float4(0.f, 0.f, 0.f, 0.f);
+          int y = -1;
+          if (row_ok) {
+            cf = A.coef[x.k.t0 + rloc];
+            y = A.y_c[x.k.t0 + rloc];
+          }
+          const int yt = y - x.k.v0 - col0;
+  #pragma unroll 1
+          for (int cc = 0; cc < BN / 64; ++cc) {
+            uint32_t pk[32];
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float v[32];
+              tmem_load_32(tcol + cc * 64 + h * 32, v);
+              if (cc == BN / 64 - 1 && h == 1) release_acc();
+              const int cb = cc * 64 + h * 32;
+              float g[32];
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float d = fmaf(v[j], A.scale, -cf.x);
+                const float pr = ex2_approx(d);
+                g[j] = -pr * fmaf(cf.y, d, cf.z);
               }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < lim) dst[j] = add ? __ldcg(dst + j) + v[j] : v[j];
+              if (static_cast<unsigned>(yt - cb) < 32u) {
+  #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j == yt - cb) g[j] += cf.w;
+              }
+              // columns past the vocabulary block hold zeros: the dh and dW
+              // tiles read whole 64-wide K steps of the scratch
+              const int lim = x.k.vact - col0 - cb;
+              if (lim < 32) {
+  #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j >= lim) g[j] = 0.f;
+              }
+  #pragma unroll
+              for (int k = 0; k < 16; ++k) pk[h * 16 + k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
+            }
+            stage_out(pk, stg0, nstore++, lrow, issuer, &A.dz_k, 1, col0 + cc * 64,
+                      x.m * PAIR_M + r128, &st->status);
+          }
+          signal(F.dz_col(x.b, xn), F.dz_all(x.b), true);
+        } else if (x.kind == U_DH) {
+          const bool scatter = A.row_map != nullptr;
+          const bool add = x.k.vb > 0;
+          const bool row_ok = rloc < x.k.rows;
+          const int64_t orow = (scatter && row_ok) ? A.row_map[x.k.t0 + rloc] : 0;
+  #pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load_32(tcol + c * 32, v);
+            if (c == BN / 32 - 1) release_acc();
+            const int cb = c * 32;
+            if (!scatter) {
+              uint32_t w[32];
+  #pragma unroll
+              for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
+              stage_out(w, stg0, nstore++, lrow, issuer, &A.dh_out, add ? 2 : 1, col0 + cb,
+                        x.k.t0 + x.m * PAIR_M + r128, &st->status);
+            } else if (row_ok) {
+              const int lim = A.H - col0 - cb;
+              float* dst = A.d_hidden + orow * A.H + col0 + cb;
+              if (lim >= 32) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+  #pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                  if (add) {
+                    // from L2: the previous value was written by another SM
+                    const float4 old = __ldcg(d4 + k);
+                    o.x += old.x;
+                    o.y += old.y;
+                    o.z += old.z;
+                    o.w += old.w;
+                  }
+                  d4[k] = o;
+                }
+              } else {
+  #pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < lim) dst[j] = add ? __ldcg(dst + j) + v[j] : v[j];
+              }
             }
           }
+          signal(F.dh_row(x.b, x.m), nullptr, !scatter);
+        } else {
+          const int mode = (x.k.tb > 0 || A.accumulate_dweight) ? 2 : 1;
+  #pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_load_32(tcol + c * 32, v);
+            if (c == BN / 32 - 1) release_acc();
+            uint32_t w[32];
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
+            stage_out(w, stg0, nstore++, lrow, issuer, &A.dw_out, mode, col0 + c * 32,
+                      x.k.v0 + x.m * PAIR_M + r128, &st->status);
+          }
+          signal(F.dw_col(x.b, x.m), nullptr, true);
         }
-        signal(F.dh_row(x.b, x.m), nullptr, !scatter);
-      } else {
-        const int mode = (x.k.tb > 0 || A.accumulate_dweight) ? 2 : 1;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_load_32(tcol + c * 32, v);
-          if (c == BN / 32 - 1) release_acc();
-          uint32_t w[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
-          stage_out(w, stg0, nstore++, lrow, issuer, &A.dw_out, mode, col0 + c * 32,
-                    x.k.v0 + x.m * PAIR_M + r128, &st->status);
-        }
-        signal(F.dw_col(x.b, x.m), nullptr, true);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (fail) break;
     }
     if (issuer) bulk_wait_all();
   }
