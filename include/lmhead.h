@@ -54,6 +54,15 @@
  *  - Calls are reentrant as long as concurrent calls use distinct
  *    workspaces.  Results are deterministic: the same inputs, shapes and
  *    chunk_size give the same bits.
+ *  - Three environment variables, read by the library, change how the work
+ *    is launched, never what is computed: LMHEAD_CTA_PAIR=0 (single-CTA
+ *    tiles instead of CTA pairs; results within the same tolerances),
+ *    LMHEAD_BWD_PERSISTENT (0: two launches per backward block, 1: one
+ *    persistent launch, 2: one launch per block window; unset: chosen by
+ *    block size; every form gives the same bits) and LMHEAD_FWD_GROUP_MB (MB
+ *    of hidden rows per group of token blocks in the forward's work order,
+ *    default 32, 0 for one group; same bits).  They are for diagnosis and
+ *    measurement.
  *  - After a kernel's first use in the process (which configures it), the
  *    compute calls make no allocation, synchronisation or configuration
  *    call, so a sequence of them can be captured in a CUDA graph.  Their
