@@ -55,6 +55,11 @@ def test_reference_arm_line():
     assert len(lines) == 1
     d = lines[0]
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+    # the same workload string as the GPU arm prints, so the two lines compare
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunked_lm_head_tcgen05_gb300 import workloads
+    assert d["config"]["workload"] == bench.workload_label(workloads.WORKLOADS["tiny"], 256)
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
@@ -66,3 +71,28 @@ def test_reference_arm_under_torchrun_prints_once():
                   str(_free_port()), "bench.py", "--impl", "reference", "--workload", "tiny",
                   "--gpus", "2", "--steps", "1", "--warmup", "1"])
     assert len(lines) == 1 and lines[0]["impl"] == "reference"
+
+
+def test_clock_record_counts_samples_inside_timed_regions_only():
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    c.samples = [(0.5, 1000.0, 500.0, 0), (1.5, 1500.0, 900.0, 0x4), (2.5, 1800.0, 1000.0, 0),
+                 (3.3, 900.0, 100.0, 0x8), (4.0, 2000.0, 50.0, 0x20)]
+    c.regions = [[1.0, 3.0, "device"], [3.2, 3.4, "e2e"]]
+    d = c.summary({"device"})
+    assert d["samples_under_load"] == 2 and d["sm_mhz"] == 1650.0
+    assert d["reasons"] == ["sw_power_cap"] and d["power_w_max"] == 1000.0
+    both = c.summary()
+    assert both["samples_under_load"] == 3 and both["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert c.region_mhz(1) == 900.0
+
+
+def test_peak_rule_burst_for_short_regions():
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks, _ = bench.measured_peaks()
+    p, kind, _ = bench.bf16_peak(0.14)
+    assert kind == "burst" and p == peaks["bf16_tflops"]
+    p, kind, _ = bench.bf16_peak(2.0)
+    assert kind == "sustained" and p == peaks["bf16_tflops_sustained"]
