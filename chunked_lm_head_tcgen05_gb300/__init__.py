@@ -23,7 +23,8 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES", "lmhead_logps_fwd_bwd", "lmhead_fwd_bwd_keeps_logits",
     "LMHEAD_OP_FWD_BWD", "LMHEAD_STRATEGY_AUTO", "LMHEAD_STRATEGY_RECOMPUTE",
     "LMHEAD_STRATEGY_KEEP_LOGITS", "lmhead_score_logits_fwd", "lmhead_score_logits_bwd",
-    "lmhead_selftest_bounded_wait",
+    "lmhead_selftest_bounded_wait", "lmhead_logps_fwd_shard", "lmhead_logps_bwd_shard",
+    "lmhead_combine_shards",
     "forward", "backward",
 ]
 
@@ -79,6 +80,13 @@ _SIGNATURES = {
                                                _VP, _VP, _VP]),
     "lmhead_score_logits_bwd": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I32, ctypes.c_float, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
+    "lmhead_logps_fwd_shard": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32,
+                                              ctypes.c_float, _I32, _VP, _VP, _SZ, _VP]),
+    "lmhead_combine_shards": (ctypes.c_int, [_VP, _I32, _VP, _VP, _I64, _I32, _VP, _VP, _VP,
+                                             _VP]),
+    "lmhead_logps_bwd_shard": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I32, _I32, _I32, _I32,
+                                              ctypes.c_float, _I32, _VP, _VP, _VP, _VP, _VP, _VP,
+                                              ctypes.c_int, _VP, _SZ, _VP]),
 }
 
 
@@ -308,6 +316,71 @@ def lmhead_score_logits_bwd(logits, targets, loss_mask, temperature, grad_logp, 
     return _on_device(tensors, stream, lambda: int(library().lmhead_score_logits_bwd(
         _ptr(logits), _ptr(targets), _ptr(loss_mask), T, V, float(temperature), _ptr(grad_logp),
         _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_logits), _stream(stream))))
+
+
+def lmhead_logps_fwd_shard(hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
+                           temperature, chunk_size, partials, workspace, stream=None):
+    """C ``lmhead_logps_fwd_shard`` on torch tensors (partials: fp32 [T, 4]); returns
+    the status code."""
+    import torch
+    T, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight_shard, "weight_shard", torch.bfloat16, (Vs, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(partials, "partials", torch.float32, (T, 4))
+    _check_workspace(workspace)
+    tensors = [hidden, weight_shard, targets, loss_mask, partials, workspace]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_fwd_shard(
+        _ptr(hidden), _ptr(weight_shard), _ptr(targets), _ptr(loss_mask), T, H, Vs,
+        int(vocab_offset), int(vocab_total), float(temperature), int(chunk_size), _ptr(partials),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))))
+
+
+def lmhead_combine_shards(partials, targets, loss_mask, vocab_total, logp, entropy, lse,
+                          stream=None):
+    """C ``lmhead_combine_shards`` (partials: fp32 [n_shards, T, 4]); returns the status."""
+    import torch
+    n, T = partials.shape[0], partials.shape[1]
+    _check_tensor(partials, "partials", torch.float32, (n, T, 4))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(logp, "logp", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    tensors = [partials, targets, loss_mask, logp, entropy, lse]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_combine_shards(
+        _ptr(partials), n, _ptr(targets), _ptr(loss_mask), T, int(vocab_total), _ptr(logp),
+        _ptr(entropy), _ptr(lse), _stream(stream))))
+
+
+def lmhead_logps_bwd_shard(hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
+                           temperature, chunk_size, grad_logp, grad_entropy, lse, entropy,
+                           d_hidden, d_weight_shard, accumulate_dweight, workspace, stream=None):
+    """C ``lmhead_logps_bwd_shard`` on torch tensors; returns the status code."""
+    import torch
+    T, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    _check_tensor(hidden, "hidden", torch.bfloat16, (T, H))
+    _check_tensor(weight_shard, "weight_shard", torch.bfloat16, (Vs, H))
+    _check_tensor(targets, "targets", torch.int32, (T,))
+    _check_tensor(loss_mask, "loss_mask", torch.uint8, (T,), allow_none=True)
+    _check_tensor(grad_logp, "grad_logp", torch.float32, (T,), allow_none=True)
+    _check_tensor(grad_entropy, "grad_entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(lse, "lse", torch.float32, (T,))
+    _check_tensor(entropy, "entropy", torch.float32, (T,), allow_none=True)
+    _check_tensor(d_hidden, "d_hidden", torch.float32, (T, H))
+    _check_tensor(d_weight_shard, "d_weight_shard", torch.float32, (Vs, H))
+    _check_workspace(workspace)
+    tensors = [hidden, weight_shard, targets, loss_mask, grad_logp, grad_entropy, lse, entropy,
+               d_hidden, d_weight_shard, workspace]
+    return _on_device(tensors, stream, lambda: int(library().lmhead_logps_bwd_shard(
+        _ptr(hidden), _ptr(weight_shard), _ptr(targets), _ptr(loss_mask), T, H, Vs,
+        int(vocab_offset), int(vocab_total), float(temperature), int(chunk_size),
+        _ptr(grad_logp), _ptr(grad_entropy), _ptr(lse), _ptr(entropy), _ptr(d_hidden),
+        _ptr(d_weight_shard), int(bool(accumulate_dweight)), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))))
 
 
 def lmhead_selftest_bounded_wait(workspace, limit_ms, stream=None):

@@ -19,10 +19,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kCompactThreads = 256;
 
-// Wrap of negative ids (y in [-V, 0) -> y + V); -1 when the id is invalid.
-__device__ __forceinline__ int wrap_target(int y, int V) {
-  if (y < 0) y += V;
-  return (y >= 0 && y < V) ? y : -1;
+// Target id of a call that holds vocabulary rows [v0, v0 + Vs) of a
+// vocabulary of Vt ids (the whole vocabulary: v0 = 0, Vs = Vt = V).  Negative
+// ids wrap (y in [-Vt, 0) -> y + Vt); a wrapped id in this call's rows becomes
+// its local row, one held by another vocabulary shard becomes kTargetElsewhere
+// (never matched by a column, no error), and an id outside [-Vt, Vt) becomes
+// kTargetInvalid.
+constexpr int kTargetInvalid = -1;
+constexpr int kTargetElsewhere = -2;
+
+__device__ __forceinline__ int shard_target(int y, int v0, int Vs, int Vt) {
+  if (y < 0) y += Vt;
+  if (y < 0 || y >= Vt) return kTargetInvalid;
+  y -= v0;
+  return (y >= 0 && y < Vs) ? y : kTargetElsewhere;
 }
 
 // Start of every call: status, scored count (known on the host only when no
@@ -81,8 +91,9 @@ __global__ void __launch_bounds__(kCompactThreads)
 
 __global__ void __launch_bounds__(kCompactThreads)
     compact_scatter_kernel(const uint8_t* __restrict__ mask, const int32_t* __restrict__ targets,
-                           int T, int V, int T_alloc, const int* __restrict__ counts, int n_chunks,
-                           int* __restrict__ idx, int* __restrict__ y_c, DeviceState* st) {
+                           int T, int v0, int Vs, int Vt, int T_alloc,
+                           const int* __restrict__ counts, int n_chunks, int* __restrict__ idx,
+                           int* __restrict__ y_c, DeviceState* st) {
   pdl_wait_prerequisites();
   pdl_launch_dependents();
   __shared__ int red[kCompactThreads / 32];
@@ -134,8 +145,8 @@ __global__ void __launch_bounds__(kCompactThreads)
     if (live & (1u << c)) {
       const int t = static_cast<int>(base) + c * kCompactThreads + threadIdx.x;
       const int pos = before + round_warp[c][w] + rank[c];
-      const int y = wrap_target(targets[t], V);
-      bad |= y < 0;
+      const int y = shard_target(targets[t], v0, Vs, Vt);
+      bad |= y == kTargetInvalid;
       idx[pos] = t;
       y_c[pos] = y;
     }
@@ -147,16 +158,16 @@ __global__ void __launch_bounds__(kCompactThreads)
   if (blockIdx.x == 0 && threadIdx.x == 0) st->rows = all;
 }
 
-__global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T, int V, int T_alloc,
-                                     int* __restrict__ y_c, DeviceState* st) {
+__global__ void targets_dense_kernel(const int32_t* __restrict__ targets, int T, int v0, int Vs,
+                                     int Vt, int T_alloc, int* __restrict__ y_c, DeviceState* st) {
   pdl_wait_prerequisites();
   pdl_launch_dependents();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= T_alloc) return;
-  int y = -1;
+  int y = kTargetInvalid;
   if (r < T) {
-    y = wrap_target(targets[r], V);
-    if (y < 0) atomicCAS(&st->status, 0, STATUS_BAD_TARGET);
+    y = shard_target(targets[r], v0, Vs, Vt);
+    if (y == kTargetInvalid) atomicCAS(&st->status, 0, STATUS_BAD_TARGET);
   }
   y_c[r] = y;
 }
@@ -180,45 +191,99 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ hidden, int H8, con
   }
 }
 
+// Outputs of unscored tokens: +0.0 (the forward's logp / entropy / lse, or a
+// vocabulary shard's partial statistics).
 __global__ void zero_masked_outputs_kernel(const uint8_t* __restrict__ mask, int T, float* logp,
-                                           float* entropy, float* lse) {
+                                           float* entropy, float* lse, float4* shard_part) {
   pdl_wait_prerequisites();
   pdl_launch_dependents();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T || mask[t]) return;
+  if (shard_part) {
+    shard_part[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
   logp[t] = 0.f;
   lse[t] = 0.f;
   if (entropy) entropy[t] = 0.f;
 }
 
-// Combine the per-split statistics (m_j, s_j, S1_j, zy_j), all in log2
-// units, by their log-sum-exp and write the token's outputs in original
-// order.  Splits are combined in a fixed order, so the result is
-// deterministic.
+// Log-sum-exp combine of n sets of statistics {m_j, s_j, S1_j, zy_j} of one
+// token over disjoint parts of the vocabulary, all in log2 units: m_j the
+// part's largest scaled logit u = z log2(e), s_j = sum 2^(u - m_j),
+// S1_j = sum 2^(u - m_j) (u - m_j), zy_j the target's u if the target lies in
+// the part, else -inf.  With M = max_j m_j and w_j = 2^(m_j - M):
+//   s = sum_j w_j s_j,  S1 = sum_j w_j (S1_j + (m_j - M) s_j),  zy = max_j zy_j.
+// The parts are taken in index order, so the result is deterministic.
+struct Stats {
+  float M, s, s1, zy;
+};
+
+__device__ __forceinline__ Stats merge_stats(const float4* __restrict__ part, int n,
+                                             int64_t stride) {
+  Stats r{-INFINITY, 0.f, 0.f, -INFINITY};
+  for (int j = 0; j < n; ++j) r.M = fmaxf(r.M, part[j * stride].x);
+  for (int j = 0; j < n; ++j) {
+    const float4 q = part[j * stride];
+    const float dm = q.x - r.M;
+    const float wgt = exp2f(dm);
+    r.s = fmaf(q.y, wgt, r.s);
+    r.s1 = fmaf(wgt, fmaf(dm, q.y, q.z), r.s1);
+    r.zy = fmaxf(r.zy, q.w);
+  }
+  return r;
+}
+
+// The forward's merge of its per-split statistics.  Writes the token's logp /
+// entropy / lse in original order (lse = (M + log2 s) ln 2, logp = (zy - M -
+// log2 s) ln 2, entropy = (log2 s - S1 / s) ln 2; NaN logp for an invalid
+// target), or, for a vocabulary shard (shard_part != NULL), the statistics
+// merged over this call's splits, which lmhead_combine_shards merges across
+// shards by the same rule.
 __global__ void fwd_merge_kernel(const float4* __restrict__ part, int n_splits, int part_ld,
                                  const int* __restrict__ idx, const int* __restrict__ y_c,
                                  const DeviceState* st, int r0, int r1, float* logp,
-                                 float* entropy, float* lse) {
+                                 float* entropy, float* lse, float4* shard_part) {
   pdl_wait_prerequisites();
   pdl_launch_dependents();
   const int r = r0 + blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= r1 || r >= st->rows) return;
-  float M = -INFINITY;
-  for (int j = 0; j < n_splits; ++j) M = fmaxf(M, part[static_cast<int64_t>(j) * part_ld + r].x);
-  float s = 0.f, s1 = 0.f, zy = -INFINITY;
-  for (int j = 0; j < n_splits; ++j) {
-    const float4 q = part[static_cast<int64_t>(j) * part_ld + r];
-    const float dm = q.x - M;
-    const float wgt = exp2f(dm);
-    s = fmaf(q.y, wgt, s);
-    s1 = fmaf(wgt, fmaf(dm, q.y, q.z), s1);
-    zy = fmaxf(zy, q.w);
-  }
-  const float l2s = log2f(s);
+  const Stats m = merge_stats(part + r, n_splits, part_ld);
   const int t = idx ? idx[r] : r;
-  lse[t] = (M + l2s) * kLn2;
-  logp[t] = y_c[r] >= 0 ? (zy - M - l2s) * kLn2 : __int_as_float(0x7fc00000);
-  if (entropy) entropy[t] = kLn2 * (l2s - s1 / s);
+  if (shard_part) {
+    shard_part[t] = make_float4(m.M, m.s, m.s1, m.zy);
+    return;
+  }
+  const float l2s = log2f(m.s);
+  lse[t] = (m.M + l2s) * kLn2;
+  logp[t] = y_c[r] >= 0 ? (m.zy - m.M - l2s) * kLn2 : __int_as_float(0x7fc00000);
+  if (entropy) entropy[t] = kLn2 * (l2s - m.s1 / m.s);
+}
+
+// Combine of vocabulary shards' statistics part[j][t] (j < n_shards, each from
+// lmhead_logps_fwd_shard over one shard) into logp / entropy / lse, as the
+// forward's merge does over its splits.  Unscored tokens give +0.0; an id
+// outside [-Vt, Vt) gives NaN logp.
+__global__ void combine_shards_kernel(const float4* __restrict__ part, int n_shards, int64_t T,
+                                      const int32_t* __restrict__ targets,
+                                      const uint8_t* __restrict__ mask, int Vt, float* logp,
+                                      float* entropy, float* lse) {
+  pdl_wait_prerequisites();
+  pdl_launch_dependents();
+  const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (t >= T) return;
+  if (mask && !mask[t]) {
+    logp[t] = 0.f;
+    lse[t] = 0.f;
+    if (entropy) entropy[t] = 0.f;
+    return;
+  }
+  const Stats m = merge_stats(part + t, n_shards, T);
+  const bool valid = shard_target(targets[t], 0, Vt, Vt) >= 0;
+  const float l2s = log2f(m.s);
+  lse[t] = (m.M + l2s) * kLn2;
+  logp[t] = valid ? (m.zy - m.M - l2s) * kLn2 : __int_as_float(0x7fc00000);
+  if (entropy) entropy[t] = kLn2 * (l2s - m.s1 / m.s);
 }
 
 // Per scored row: {lse * log2 e, g_e ln2 / tau, (g_l + g_e H) / tau, g_l / tau}
@@ -357,20 +422,21 @@ cudaError_t launch_clear_state(DeviceState* st, int rows_if_dense, int* counters
 
 int compact_chunks(int T) { return (T + kCompactChunk - 1) / kCompactChunk; }
 
-cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
-                           int* counts, int* idx, int* y_c, DeviceState* st, cudaStream_t s) {
+cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int v0, int Vs,
+                           int Vt, int T_alloc, int* counts, int* idx, int* y_c, DeviceState* st,
+                           cudaStream_t s) {
   const int n = compact_chunks(T);
   if (n < 1) return cudaSuccess;
   const cudaError_t e = launch_pdl(compact_count_kernel, n, kCompactThreads, s, mask, T, counts);
   if (e != cudaSuccess) return e;
-  return launch_pdl(compact_scatter_kernel, n, kCompactThreads, s, mask, targets, T, V, T_alloc,
-                    static_cast<const int*>(counts), n, idx, y_c, st);
+  return launch_pdl(compact_scatter_kernel, n, kCompactThreads, s, mask, targets, T, v0, Vs, Vt,
+                    T_alloc, static_cast<const int*>(counts), n, idx, y_c, st);
 }
 
-cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
-                                 DeviceState* st, cudaStream_t s) {
-  return launch_pdl(targets_dense_kernel, (T_alloc + 255) / 256, 256, s, targets, T, V, T_alloc,
-                    y_c, st);
+cudaError_t launch_targets_dense(const int32_t* targets, int T, int v0, int Vs, int Vt,
+                                 int T_alloc, int* y_c, DeviceState* st, cudaStream_t s) {
+  return launch_pdl(targets_dense_kernel, (T_alloc + 255) / 256, 256, s, targets, T, v0, Vs, Vt,
+                    T_alloc, y_c, st);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
@@ -382,17 +448,25 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, in
 }
 
 cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
-                                       float* lse, cudaStream_t s) {
+                                       float* lse, float4* shard_part, cudaStream_t s) {
   return launch_pdl(zero_masked_outputs_kernel, (T + 255) / 256, 256, s, mask, T, logp, entropy,
-                    lse);
+                    lse, shard_part);
 }
 
 cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
                              const int* y_c, const DeviceState* st, int r0, int r1, float* logp,
-                             float* entropy, float* lse, cudaStream_t s) {
+                             float* entropy, float* lse, float4* shard_part, cudaStream_t s) {
   if (r1 <= r0) return cudaSuccess;
   return launch_pdl(fwd_merge_kernel, (r1 - r0 + 255) / 256, 256, s, partials, n_splits, part_ld,
-                    idx, y_c, st, r0, r1, logp, entropy, lse);
+                    idx, y_c, st, r0, r1, logp, entropy, lse, shard_part);
+}
+
+cudaError_t launch_combine_shards(const float4* partials, int n_shards, int64_t T,
+                                  const int32_t* targets, const uint8_t* mask, int Vt, float* logp,
+                                  float* entropy, float* lse, cudaStream_t s) {
+  const int64_t blocks = (T + 255) / 256;
+  return launch_pdl(combine_shards_kernel, static_cast<int>(blocks), 256, s, partials, n_shards,
+                    T, targets, mask, Vt, logp, entropy, lse);
 }
 
 cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r1, const float* lse,

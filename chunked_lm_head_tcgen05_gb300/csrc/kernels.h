@@ -162,18 +162,32 @@ cudaError_t launch_gemm_fwd_z(const LaunchArgs& a, int grid, bool pair, cudaStre
 // int per chunk (compact_chunks(T) of them).
 constexpr int kCompactChunk = 4096;
 int compact_chunks(int T);
-cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int V, int T_alloc,
-                           int* counts, int* idx, int* y_c, DeviceState* st, cudaStream_t s);
-cudaError_t launch_targets_dense(const int32_t* targets, int T, int V, int T_alloc, int* y_c,
-                                 DeviceState* st, cudaStream_t s);
+// Targets are ids of a vocabulary of Vt entries; the call holds rows
+// [v0, v0 + Vs) of it (the whole vocabulary: v0 = 0, Vs = Vt).  y_c gets the
+// local row of each scored target, -2 for a valid id held by another
+// vocabulary shard, -1 for an invalid id (which also sets the status word).
+cudaError_t launch_compact(const uint8_t* mask, const int32_t* targets, int T, int v0, int Vs,
+                           int Vt, int T_alloc, int* counts, int* idx, int* y_c, DeviceState* st,
+                           cudaStream_t s);
+cudaError_t launch_targets_dense(const int32_t* targets, int T, int v0, int Vs, int Vt,
+                                 int T_alloc, int* y_c, DeviceState* st, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* hidden, int H, const int* idx, int T_alloc,
                                const DeviceState* st, uint16_t* h_c, cudaStream_t s);
+// Unscored tokens' outputs +0.0: logp / entropy / lse, or, when shard_part
+// is not NULL, only the shard's partial statistics.
 cudaError_t launch_zero_masked_outputs(const uint8_t* mask, int T, float* logp, float* entropy,
-                                       float* lse, cudaStream_t s);
-// Rows [r0, r1) of the compacted order (clipped to the scored count).
+                                       float* lse, float4* shard_part, cudaStream_t s);
+// Rows [r0, r1) of the compacted order (clipped to the scored count).  With
+// shard_part != NULL the merged statistics {m, s, S1, zy} (log2 units) go
+// there, in token order, instead of logp / entropy / lse.
 cudaError_t launch_fwd_merge(const float4* partials, int n_splits, int part_ld, const int* idx,
                              const int* y_c, const DeviceState* st, int r0, int r1, float* logp,
-                             float* entropy, float* lse, cudaStream_t s);
+                             float* entropy, float* lse, float4* shard_part, cudaStream_t s);
+// logp / entropy / lse of T tokens from n_shards sets of shard statistics
+// partials[j][t] (token order); Vt is the whole vocabulary's size.
+cudaError_t launch_combine_shards(const float4* partials, int n_shards, int64_t T,
+                                  const int32_t* targets, const uint8_t* mask, int Vt, float* logp,
+                                  float* entropy, float* lse, cudaStream_t s);
 // Rows [r0, r1): coefficients of scored rows, zeros past the scored count.
 cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r1, const float* lse,
                             const float* entropy, const float* grad_logp,

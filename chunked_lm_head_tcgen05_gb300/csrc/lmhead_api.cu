@@ -462,8 +462,11 @@ struct Front {
   int64_t T_alloc;
 };
 
+// The call holds vocabulary rows [v0, v0 + V) of a vocabulary of Vt ids
+// (v0 = 0, Vt = V outside the vocabulary-sharded calls).
 lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_t* mask, int64_t T,
-                    int32_t H, int32_t V, char* ws, const Layout& L, cudaStream_t s, Front* f) {
+                    int32_t H, int32_t V, int32_t v0, int32_t Vt, char* ws, const Layout& L,
+                    cudaStream_t s, Front* f) {
   f->T_alloc = round_up(T, BM);
   f->st = reinterpret_cast<DeviceState*>(ws + L.state);
   f->y_c = reinterpret_cast<int*>(ws + L.y_c);
@@ -476,8 +479,8 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
     f->idx = reinterpret_cast<int*>(ws + L.idx);
     uint16_t* h_c = reinterpret_cast<uint16_t*>(ws + L.h_c);
     LMH_TRY(launch("compact", s, [&] {
-      return launch_compact(mask, targets, Ti, V, Ta, reinterpret_cast<int*>(ws + L.chunk_counts),
-                            f->idx, f->y_c, f->st, s);
+      return launch_compact(mask, targets, Ti, v0, V, Vt, Ta,
+                            reinterpret_cast<int*>(ws + L.chunk_counts), f->idx, f->y_c, f->st, s);
     }));
     LMH_TRY(launch("gather_rows", s, [&] {
       return launch_gather_rows(hidden, H, f->idx, Ta, f->st, h_c, s);
@@ -487,7 +490,7 @@ lmhead_status front(const uint16_t* hidden, const int32_t* targets, const uint8_
   } else {
     f->idx = nullptr;
     LMH_TRY(launch("targets_dense", s, [&] {
-      return launch_targets_dense(targets, Ti, V, Ta, f->y_c, f->st, s);
+      return launch_targets_dense(targets, Ti, v0, V, Vt, Ta, f->y_c, f->st, s);
     }));
     f->h_src = hidden;
     f->rows_avail = T;
@@ -539,15 +542,24 @@ lmhead_status lmhead_plan_info(int64_t T, int32_t H, int32_t V, int32_t chunk_si
   return LMHEAD_OK;
 }
 
-lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
-                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
-                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
-                               float* logp, float* entropy, float* lse, void* workspace,
-                               size_t workspace_bytes, lmhead_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward over vocabulary rows [v0, v0 + V) of a vocabulary of Vt ids.  With
+// shard_part == NULL (the whole vocabulary: v0 = 0, Vt = V) it writes logp /
+// entropy / lse; otherwise the token's statistics over these rows go to
+// shard_part, for lmhead_combine_shards.
+lmhead_status fwd_impl(const uint16_t* hidden, const uint16_t* weight, const int32_t* targets,
+                       const uint8_t* loss_mask, int64_t T, int32_t H, int32_t V, int32_t v0,
+                       int32_t Vt, float temperature, int32_t chunk_size, float* logp,
+                       float* entropy, float* lse, float4* shard_part, void* workspace,
+                       size_t workspace_bytes, lmhead_stream_t stream) {
   lmhead_status rc = check_sizes(T, H, V, temperature, chunk_size);
   if (rc != LMHEAD_OK) return rc;
   if (T == 0) return LMHEAD_OK;
-  if (!hidden || !weight || !targets || !logp || !lse || !workspace) return LMHEAD_ERR_INVALID_ARG;
+  if (!hidden || !weight || !targets || !workspace || (!shard_part && (!logp || !lse)))
+    return LMHEAD_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(weight) || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return LMHEAD_ERR_UNSUPPORTED;
   const Layout L = layout(LMHEAD_OP_FWD, T, H, V, chunk_size);
@@ -558,7 +570,7 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   char* ws = static_cast<char*>(workspace);
 
   Front f;
-  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  rc = front(hidden, targets, loss_mask, T, H, V, v0, Vt, ws, L, s, &f);
   if (rc != LMHEAD_OK) return rc;
 
   const bool pair = use_pair();
@@ -590,23 +602,27 @@ lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
   LMH_TRY(launch("fwd_stats_gemm", s, [&] { return launch_gemm_fwd_stats(la, grid, pair, s); }));
   LMH_TRY(launch("fwd_merge", s, [&] {
     return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st, 0,
-                            static_cast<int>(f.T_alloc), logp, entropy, lse, s);
+                            static_cast<int>(f.T_alloc), logp, entropy, lse, shard_part, s);
   }));
   if (loss_mask) {
     LMH_TRY(launch("zero_masked_outputs", s, [&] {
-      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse, s);
+      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse,
+                                        shard_part, s);
     }));
   }
   return LMHEAD_OK;
 }
 
-lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
-                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
-                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
-                               const float* grad_logp, const float* grad_entropy,
-                               const float* lse, const float* entropy, float* d_hidden,
-                               float* d_weight, int accumulate_dweight, void* workspace,
-                               size_t workspace_bytes, lmhead_stream_t stream) {
+// Backward over vocabulary rows [v0, v0 + V) of a vocabulary of Vt ids, given
+// the whole vocabulary's lse (and entropy): d_hidden gets these rows' share of
+// the gradient, d_weight the gradient of these rows.
+lmhead_status bwd_impl(const uint16_t* hidden, const uint16_t* weight, const int32_t* targets,
+                       const uint8_t* loss_mask, int64_t T, int32_t H, int32_t V, int32_t v0,
+                       int32_t Vt, float temperature, int32_t chunk_size,
+                       const float* grad_logp, const float* grad_entropy, const float* lse,
+                       const float* entropy, float* d_hidden, float* d_weight,
+                       int accumulate_dweight, void* workspace, size_t workspace_bytes,
+                       lmhead_stream_t stream) {
   lmhead_status rc = check_sizes(T, H, V, temperature, chunk_size);
   if (rc != LMHEAD_OK) return rc;
   if (!weight || !d_weight) return LMHEAD_ERR_INVALID_ARG;
@@ -629,7 +645,7 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   char* ws = static_cast<char*>(workspace);
 
   Front f;
-  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  rc = front(hidden, targets, loss_mask, T, H, V, v0, Vt, ws, L, s, &f);
   if (rc != LMHEAD_OK) return rc;
 
   float4* coef = reinterpret_cast<float4*>(ws + L.coef);
@@ -801,6 +817,88 @@ lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
   return LMHEAD_OK;
 }
 
+// Arguments of the vocabulary-sharded calls: rows [vocab_offset, vocab_offset +
+// V_shard) of a vocabulary of vocab_total ids.
+lmhead_status check_shard(int32_t V_shard, int32_t vocab_offset, int32_t vocab_total) {
+  if (V_shard <= 0 || vocab_offset < 0 || vocab_total <= 0 ||
+      static_cast<int64_t>(vocab_offset) + V_shard > vocab_total)
+    return LMHEAD_ERR_INVALID_ARG;
+  return LMHEAD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lmhead_status lmhead_logps_fwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               float* logp, float* entropy, float* lse, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream) {
+  return fwd_impl(hidden, weight, targets, loss_mask, T, H, V, 0, V, temperature, chunk_size,
+                  logp, entropy, lse, nullptr, workspace, workspace_bytes, stream);
+}
+
+lmhead_status lmhead_logps_bwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                               int32_t H, int32_t V, float temperature, int32_t chunk_size,
+                               const float* grad_logp, const float* grad_entropy,
+                               const float* lse, const float* entropy, float* d_hidden,
+                               float* d_weight, int accumulate_dweight, void* workspace,
+                               size_t workspace_bytes, lmhead_stream_t stream) {
+  return bwd_impl(hidden, weight, targets, loss_mask, T, H, V, 0, V, temperature, chunk_size,
+                  grad_logp, grad_entropy, lse, entropy, d_hidden, d_weight, accumulate_dweight,
+                  workspace, workspace_bytes, stream);
+}
+
+lmhead_status lmhead_logps_fwd_shard(const uint16_t* hidden, const uint16_t* weight_shard,
+                                     const int32_t* targets, const uint8_t* loss_mask,
+                                     int64_t T, int32_t H, int32_t V_shard, int32_t vocab_offset,
+                                     int32_t vocab_total, float temperature, int32_t chunk_size,
+                                     float* partials, void* workspace, size_t workspace_bytes,
+                                     lmhead_stream_t stream) {
+  lmhead_status rc = check_shard(V_shard, vocab_offset, vocab_total);
+  if (rc != LMHEAD_OK) return rc;
+  if (T > 0 && !partials) return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(partials)) return LMHEAD_ERR_UNSUPPORTED;
+  return fwd_impl(hidden, weight_shard, targets, loss_mask, T, H, V_shard, vocab_offset,
+                  vocab_total, temperature, chunk_size, nullptr, nullptr, nullptr,
+                  reinterpret_cast<float4*>(partials), workspace, workspace_bytes, stream);
+}
+
+lmhead_status lmhead_logps_bwd_shard(const uint16_t* hidden, const uint16_t* weight_shard,
+                                     const int32_t* targets, const uint8_t* loss_mask,
+                                     int64_t T, int32_t H, int32_t V_shard, int32_t vocab_offset,
+                                     int32_t vocab_total, float temperature, int32_t chunk_size,
+                                     const float* grad_logp, const float* grad_entropy,
+                                     const float* lse, const float* entropy, float* d_hidden,
+                                     float* d_weight_shard, int accumulate_dweight,
+                                     void* workspace, size_t workspace_bytes,
+                                     lmhead_stream_t stream) {
+  const lmhead_status rc = check_shard(V_shard, vocab_offset, vocab_total);
+  if (rc != LMHEAD_OK) return rc;
+  return bwd_impl(hidden, weight_shard, targets, loss_mask, T, H, V_shard, vocab_offset,
+                  vocab_total, temperature, chunk_size, grad_logp, grad_entropy, lse, entropy,
+                  d_hidden, d_weight_shard, accumulate_dweight, workspace, workspace_bytes,
+                  stream);
+}
+
+lmhead_status lmhead_combine_shards(const float* partials, int32_t n_shards,
+                                    const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                                    int32_t vocab_total, float* logp, float* entropy, float* lse,
+                                    lmhead_stream_t stream) {
+  if (n_shards <= 0 || T < 0 || vocab_total <= 0) return LMHEAD_ERR_INVALID_ARG;
+  if (T >= (int64_t{1} << 31) - 256) return LMHEAD_ERR_UNSUPPORTED;
+  if (T == 0) return LMHEAD_OK;
+  if (!partials || !targets || !logp || !lse) return LMHEAD_ERR_INVALID_ARG;
+  if (!aligned16(partials)) return LMHEAD_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  LMH_TRY(launch("combine_shards", s, [&] {
+    return launch_combine_shards(reinterpret_cast<const float4*>(partials), n_shards, T, targets,
+                                 loss_mask, vocab_total, logp, entropy, lse, s);
+  }));
+  return LMHEAD_OK;
+}
 
 lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weight,
                                    const int32_t* targets, const uint8_t* loss_mask, int64_t T,
@@ -848,11 +946,12 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
   char* ws = static_cast<char*>(workspace);
   const Layout L = layout(LMHEAD_OP_FWD_BWD, T, H, V, chunk_size);
   Front f;
-  rc = front(hidden, targets, loss_mask, T, H, V, ws, L, s, &f);
+  rc = front(hidden, targets, loss_mask, T, H, V, 0, V, ws, L, s, &f);
   if (rc != LMHEAD_OK) return rc;
   if (loss_mask) {
     LMH_TRY(launch("zero_masked_outputs", s, [&] {
-      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse, s);
+      return launch_zero_masked_outputs(loss_mask, static_cast<int>(T), logp, entropy, lse,
+                                        nullptr, s);
     }));
     LMH_TRY(launch("zero_masked_rows", s, [&] {
       return launch_zero_masked_rows(loss_mask, static_cast<int>(T), H, d_hidden, s);
@@ -910,7 +1009,7 @@ lmhead_status lmhead_logps_fwd_bwd(const uint16_t* hidden, const uint16_t* weigh
     const int r0 = static_cast<int>(t0), r1 = static_cast<int>(t0 + m_cap);
     LMH_TRY(launch("fwd_merge", s, [&] {
       return launch_fwd_merge(part, splits, static_cast<int>(f.T_alloc), f.idx, f.y_c, f.st, r0,
-                              r1, logp, entropy, lse, s);
+                              r1, logp, entropy, lse, nullptr, s);
     }));
     LMH_TRY(launch("bwd_prep", s, [&] {
       return launch_bwd_prep(f.idx, f.st, r0, r1, lse, entropy, grad_logp, grad_entropy,

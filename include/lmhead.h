@@ -214,6 +214,85 @@ int lmhead_fwd_bwd_keeps_logits(int64_t T, int32_t H, int32_t V, int32_t chunk_s
                                 int32_t* block_tokens);
 
 /*
+ * Vocabulary-sharded head.  The vocabulary table is split by rows into
+ * shards; a call holds rows [vocab_offset, vocab_offset + V_shard) of a
+ * vocabulary of vocab_total ids (weight_shard [V_shard, H] bf16 is those rows,
+ * for instance a view into the whole table, or one GPU's shard of it).  A
+ * token's statistics over disjoint parts of the vocabulary combine exactly by
+ * their log-sum-exp (the rule by which the "Long Sequences (SeCO)" guide,
+ * section "Efficiency", merges partial attention results, and by which the
+ * forward merges its own vocabulary splits), so the head over the whole
+ * vocabulary is:
+ *   1. lmhead_logps_fwd_shard on every shard -> 16 bytes of statistics per
+ *      token and shard;
+ *   2. the shards' statistics brought together (on several GPUs: one
+ *      all-gather of 16 bytes per token), and lmhead_combine_shards -> logp,
+ *      entropy, lse of the whole vocabulary, as lmhead_logps_fwd gives them;
+ *   3. lmhead_logps_bwd_shard on every shard with that lse and entropy ->
+ *      the shard's rows of d_weight and its share of d_hidden; d_hidden is the
+ *      sum of the shares (on several GPUs: one all-reduce).
+ * The shards must tile [0, vocab_total) without overlap.  Results agree with
+ * the unsharded calls within the head's tolerances (fp32 summation order
+ * differs), not bit for bit.
+ *
+ * lmhead_logps_fwd_shard: arguments as lmhead_logps_fwd with V = V_shard, plus
+ *  targets      ids of the whole vocabulary: ids in [-vocab_total, 0) wrap to
+ *               id + vocab_total; an id held by another shard is no error; a
+ *               scored id outside [-vocab_total, vocab_total) sets
+ *               LMHEAD_ERR_BAD_TARGET in the device status
+ *  partials     [T][4] fp32 out, 16-byte aligned: per token {m, s, S1, zy} in
+ *               base-2 units of u = z log2(e) over this shard's rows: m the
+ *               largest u, s = sum 2^(u - m), S1 = sum 2^(u - m) (u - m), zy the
+ *               target's u if the target is in this shard, else -inf.
+ *               Unscored tokens get zeros.
+ *  workspace    lmhead_workspace_size(LMHEAD_OP_FWD, T, H, V_shard, chunk_size)
+ * LMHEAD_ERR_INVALID_ARG also for V_shard <= 0, vocab_offset < 0 or
+ * vocab_offset + V_shard > vocab_total; LMHEAD_ERR_UNSUPPORTED for partials
+ * not 16-byte aligned.
+ */
+lmhead_status lmhead_logps_fwd_shard(const uint16_t* hidden, const uint16_t* weight_shard,
+                                     const int32_t* targets, const uint8_t* loss_mask,
+                                     int64_t T, int32_t H, int32_t V_shard, int32_t vocab_offset,
+                                     int32_t vocab_total, float temperature, int32_t chunk_size,
+                                     float* partials, void* workspace, size_t workspace_bytes,
+                                     lmhead_stream_t stream);
+
+/*
+ * logp, entropy (NULL to skip) and lse [T] fp32 of the whole vocabulary from
+ * n_shards sets of shard statistics, partials [n_shards][T][4] fp32 (16-byte
+ * aligned; set j from lmhead_logps_fwd_shard on shard j, in any fixed shard
+ * order: the result depends on the order only through fp32 rounding).
+ * Unscored tokens (loss_mask 0) give +0.0; a scored id outside
+ * [-vocab_total, vocab_total) gives logp = NaN.  HBM-bound: one read of the
+ * statistics.
+ */
+lmhead_status lmhead_combine_shards(const float* partials, int32_t n_shards,
+                                    const int32_t* targets, const uint8_t* loss_mask, int64_t T,
+                                    int32_t vocab_total, float* logp, float* entropy, float* lse,
+                                    lmhead_stream_t stream);
+
+/*
+ * Backward of one vocabulary shard: arguments as lmhead_logps_bwd with
+ * V = V_shard and targets as in lmhead_logps_fwd_shard, given the WHOLE
+ * vocabulary's lse (and entropy, with grad_entropy) from lmhead_combine_shards.
+ *  d_hidden        [T, H] fp32 out, overwritten: this shard's share,
+ *                  sum over v in the shard of (dz_v / tau) W_v; the gradient of
+ *                  hidden is the sum of every shard's share
+ *  d_weight_shard  [V_shard, H] fp32: the gradient of this shard's rows,
+ *                  overwritten or accumulated as in lmhead_logps_bwd
+ *  workspace       lmhead_workspace_size(LMHEAD_OP_BWD, T, H, V_shard, chunk_size)
+ */
+lmhead_status lmhead_logps_bwd_shard(const uint16_t* hidden, const uint16_t* weight_shard,
+                                     const int32_t* targets, const uint8_t* loss_mask,
+                                     int64_t T, int32_t H, int32_t V_shard, int32_t vocab_offset,
+                                     int32_t vocab_total, float temperature, int32_t chunk_size,
+                                     const float* grad_logp, const float* grad_entropy,
+                                     const float* lse, const float* entropy, float* d_hidden,
+                                     float* d_weight_shard, int accumulate_dweight,
+                                     void* workspace, size_t workspace_bytes,
+                                     lmhead_stream_t stream);
+
+/*
  * Logits-level scoring, for callers that already hold one chunk's logits
  * (the per-chunk cross-entropy of a chunked trainer; "Long Sequences (SeCO)"
  * guide, section "Efficiency").  logits [T, V] fp32 row-major; the scored
@@ -277,7 +356,8 @@ int64_t lmhead_read_scored_count(const void* workspace, lmhead_stream_t stream);
 
 /*
  * Size of the static device scratch that lmhead_logps_fwd_noalloc uses:
- * 64 MiB, held on every GPU that loads this library until the process exits.
+ * 64 MiB on every GPU where the library's module is loaded, held until the
+ * process exits.
  */
 #define LMHEAD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -288,17 +368,22 @@ int64_t lmhead_read_scored_count(const void* workspace, lmhead_stream_t stream);
  * cudaMalloc would synchronise the device and stall other work.  The pages
  * have no counterpart to this entry point; it exists only for such callers.
  *
- * Same arguments, results and errors as lmhead_logps_fwd, minus the
- * workspace: the scratch comes from one file-scope device array of
- * LMHEAD_NOALLOC_SCRATCH_BYTES per GPU.  It allocates nothing (no cudaMalloc,
- * no cudaFree, no allocating library call).
- *  - Sizes whose forward workspace (lmhead_workspace_size(LMHEAD_OP_FWD,
- *    ...)) exceeds LMHEAD_NOALLOC_SCRATCH_BYTES are rejected with
- *    LMHEAD_ERR_WORKSPACE_TOO_SMALL before anything is launched (about
- *    11,000 tokens at H = 2560).
- *  - The first call on a device looks up the array's device address on the
- *    current device (cudaGetSymbolAddress) and caches it; make that first
- *    call before any stream capture.
+ * Same arguments and results as lmhead_logps_fwd, minus the workspace: the
+ * scratch comes from one file-scope device array of
+ * LMHEAD_NOALLOC_SCRATCH_BYTES per GPU.  The call allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library call).
+ *  - Errors are those of lmhead_logps_fwd, checked in the same order (sizes,
+ *    pointers, alignment); sizes whose forward workspace
+ *    (lmhead_workspace_size(LMHEAD_OP_FWD, ...)) exceeds
+ *    LMHEAD_NOALLOC_SCRATCH_BYTES then return LMHEAD_ERR_WORKSPACE_TOO_SMALL
+ *    before anything is launched (about 11,000 tokens at H = 2560).
+ *  - Set-up happens in the first call on each device (and in each CUDA
+ *    context on it): the call looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress) and caches it per context.  With
+ *    CUDA's default lazy module loading that lookup also loads the library's
+ *    module, which is when the array's memory is taken, so the first call can
+ *    fail with LMHEAD_ERR_CUDA when the device lacks that much free memory.
+ *    Make the first call at set-up time, before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous
  *    call's contents; each call re-initialises the parts that must start
  *    from a known state.  Calls whose work overlaps on the GPU (different

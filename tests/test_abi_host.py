@@ -174,3 +174,51 @@ def test_plan_is_chunk_bounded(lib):
         assert tb % 256 == 0 and vb % 256 == 0
         assert tb * vb <= max(c * V, 256 * 256) + 256 * 256 + 256 * tb + 256 * vb, (T, V, c, tb, vb)
         assert tb <= (T + 255) // 256 * 256
+
+
+def test_shard_argument_errors(lib):
+    f = lib.lmhead_logps_fwd_shard
+    b = lib.lmhead_logps_bwd_shard
+    cmb = lib.lmhead_combine_shards
+    A = _fake(1 << 20)
+    ws = _fake(1 << 24)
+
+    def fwd(h=A, w=A, y=A, m=None, T=8, H=64, Vs=10, v0=0, Vt=30, tau=1.0, c=4, part=A, wsp=ws,
+            wsb=1 << 40):
+        return f(h, w, y, m, T, H, Vs, v0, Vt, tau, c, part, wsp, wsb, None)
+
+    def bwd(h=A, w=A, y=A, m=None, T=8, H=64, Vs=10, v0=0, Vt=30, tau=1.0, c=4, gl=A, ge=None,
+            ls=A, en=None, dh=A, dw=A, acc=0, wsp=ws, wsb=1 << 40):
+        return b(h, w, y, m, T, H, Vs, v0, Vt, tau, c, gl, ge, ls, en, dh, dw, acc, wsp, wsb,
+                 None)
+
+    assert fwd(Vs=0) == 1
+    assert fwd(v0=-1) == 1
+    assert fwd(v0=21) == 1                 # rows past the vocabulary
+    assert fwd(Vt=0) == 1
+    assert fwd(part=None) == 1
+    assert fwd(part=_fake((1 << 20) + 8)) == 2   # statistics need 16-byte alignment
+    assert fwd(tau=0.0) == 1
+    assert fwd(H=96) == 2
+    assert fwd(h=None) == 1
+    assert fwd(wsb=16) == 3
+    assert fwd(T=0, h=None, w=None, y=None, part=None, wsp=None) == 0
+    assert bwd(v0=25) == 1
+    assert bwd(Vs=-2) == 1
+    assert bwd(ge=A, en=None) == 1
+    assert bwd(dw=None) == 1
+    assert bwd(wsb=100) == 3
+    assert bwd(T=0, acc=1, h=None, y=None, ls=None, dh=None, wsp=None) == 0
+
+    def comb(part=A, n=2, y=A, m=None, T=8, Vt=30, lp=A, en=None, ls=A):
+        return cmb(part, n, y, m, T, Vt, lp, en, ls, None)
+
+    assert comb(n=0) == 1
+    assert comb(T=-1) == 1
+    assert comb(Vt=0) == 1
+    assert comb(part=None) == 1
+    assert comb(lp=None) == 1
+    assert comb(ls=None) == 1
+    assert comb(y=None) == 1
+    assert comb(part=_fake((1 << 20) + 4)) == 2
+    assert comb(T=0, part=None, y=None, lp=None, ls=None) == 0
