@@ -890,6 +890,51 @@ def run_ours(args, rank, world, local):
         "plan": {"fwd_splits": splits, "bwd_tokens": tb_rows, "bwd_vocab": vb_cols},
     }
 
+    # ---- the step as two vocabulary shards run in turn on this GPU and combined (what two
+    # GPUs would each run, minus the all-gather of the statistics and the all-reduce of the
+    # d_hidden shares)
+    vocab_shards = None
+    try:
+        half = (V // 2 + 255) // 256 * 256
+        bounds = [(0, half), (half, V)]
+        parts = torch.empty((2, T, 4), device=dev)
+        shares = [torch.empty((T, H), device=dev) for _ in bounds]
+        ws_sh = torch.empty(max(lm.lmhead_workspace_size(op, T, H, b - a, c)
+                                for op in (0, 1) for a, b in bounds), dtype=torch.uint8,
+                            device=dev)
+
+        def shard_step():
+            rc = 0
+            for j, (a, b) in enumerate(bounds):
+                rc |= lm.lmhead_logps_fwd_shard(g["hidden"], g["weight"][a:b], g["targets"],
+                                                g["loss_mask"], a, V, tau, c, parts[j], ws_sh,
+                                                stream)
+            rc |= lm.lmhead_combine_shards(parts, g["targets"], g["loss_mask"], V, hd.logp,
+                                           hd.ent, hd.lse, stream)
+            for j, (a, b) in enumerate(bounds):
+                rc |= lm.lmhead_logps_bwd_shard(g["hidden"], g["weight"][a:b], g["targets"],
+                                                g["loss_mask"], a, V, tau, c, g["grad_logp"],
+                                                g["grad_entropy"], hd.lse, hd.ent, shares[j],
+                                                hd.dw[a:b], 0, ws_sh, stream)
+            if rc:
+                raise lm.LmheadError(rc, "shard step")
+
+        shard_step()
+        t_sh, t_un = [], []
+        for _ in range(3):   # alternating with the unsharded step, at the same clocks
+            t_sh.append(timer(shard_step, nb, "vocab_shards")[0] / nb)
+            t_un.append(timer(hd.step, nb, "vocab_shards_ref")[0] / nb)
+        tsh, tun = median(t_sh), median(t_un)
+        vocab_shards = {"shards": [list(b) for b in bounds], "ms_per_step": tsh * 1e3,
+                        "unsharded_ms_per_step_interleaved": tun * 1e3,
+                        "tokens_per_s": Tv * world / tsh,
+                        "note": "two shards' calls in turn on one GPU plus the combine; the "
+                                "all-gather of 16 B/token and the all-reduce of d_hidden that "
+                                "two GPUs would add are not included"}
+        del parts, shares, ws_sh
+    except Exception as exc:   # report, do not fail the bench
+        vocab_shards = {"error": str(exc)[:200]}
+
     # ---- the same step captured once in a CUDA graph and replayed (launch overhead removed)
     graph_replay = None
     try:
@@ -976,6 +1021,7 @@ def run_ours(args, rank, world, local):
         "kernels": kernels,
         "breakdown": breakdown,
         "graph_replay": graph_replay,
+        "vocab_shards": vocab_shards,
         "memory": memory,
         "cublas_same_shape": cublas,
     }
