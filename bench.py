@@ -624,8 +624,9 @@ def roofline_of(per, steps, Tv, H, V, region_s, workload):
     launch_s = dms / dl / 1e3
     achieved = flops_per_launch / launch_s / 1e12
     peak, kind, src = bf16_peak(region_s)
+    burst, _, _ = bf16_peak(0.0)
     return {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-            "unit": "TFLOP/s", "frac": achieved / peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst_peak": achieved / burst,
             "traffic": recorded_traffic(dom, workload),
             "peak_kind": kind, "peak_source": src, "timed_region_s": region_s,
             "flops_per_launch": flops_per_launch, "launches_per_step": launches_per_step,
@@ -694,7 +695,7 @@ def measure_workload(lm, name, args, world, dev, stream, clocks, timer, cpu=True
     res["fwd"] = {"ms": f * 1e3, "tokens_per_s": Tv * world / f,
                   "tflops": 2.0 * Tv * H * V / f / 1e12}
     # dominant kernel of the fwd + bwd step
-    nk = max(3, k // 2)
+    nk = max(3, k // 2, min(400, int(math.ceil(SUSTAINED_REGION_S / max(ms, 1e-6)))))
     per, treg = kernel_profile(lm, timer, hd.step, nk, name + ":profile")
     res["roofline"] = roofline_of(per, nk, Tv, H, V, treg, name)
     res["kernels"] = kernel_shares(per, nk)
@@ -847,8 +848,9 @@ def run_ours(args, rank, world, local):
     clk = clocks.summary({"device", "e2e"})
     clk_dev = clocks.summary({"device"})
 
-    # ---- per-kernel durations (CUDA events around each launch, same stream)
-    nprof = max(3, K // 4)
+    # ---- per-kernel durations (CUDA events around each launch, same stream), over a
+    # region of at least a second: the power-capped steady state, against the sustained peak
+    nprof = max(3, K // 4, min(400, int(math.ceil(SUSTAINED_REGION_S / max(t_med / K, 1e-6)))))
     per, treg = kernel_profile(lm, timer, hd.step, nprof, "profile")
     roofline = roofline_of(per, nprof, Tv, H, V, treg, args.workload)
     kernels = kernel_shares(per, nprof)
@@ -1007,6 +1009,7 @@ def run_ours(args, rank, world, local):
         "tflops_executed": 8.0 * Tv * H * V * world / step_s / 1e12,
         "frac_peak_counted": counted / step_s / 1e12 / step_peak,
         "frac_peak_executed": 8.0 * Tv * H * V / step_s / 1e12 / step_peak,
+        "frac_peak_counted_of_sustained": counted / step_s / 1e12 / bf16_peak(1e9)[0],
         "step_peak": {"tflops": step_peak, "kind": step_kind, "source": step_src,
                       "timed_region_s": t_med},
         "clocks": clk,
