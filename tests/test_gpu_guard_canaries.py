@@ -10,8 +10,9 @@ in tokens, hidden size and vocabulary, with masked rows, so partial tiles,
 partial K steps and the masked-row paths all run. Every entry point that
 writes device memory is covered: the forward, the backward in its
 persistent and per-block forms (with and without accumulation), the single
-call in both strategies, the logits-level scoring pair, and the forward
-without a workspace.
+call in both strategies, the logits-level scoring pair, the forward
+without a workspace, and the vocabulary-sharded forward, combine and
+backward.
 """
 import os
 
@@ -195,3 +196,47 @@ def test_score_logits_stays_in_bounds(V):
     assert rc == 0
     _check(dict(gin, lse=out["lse"], entropy=out["entropy"]), {"d_logits": d},
            "lmhead_score_logits_bwd")
+
+
+@pytest.mark.parametrize("ci", range(len(CASES)))
+def test_vocabulary_shards_stay_in_bounds(ci):
+    """Each shard's table rows, statistics, d_hidden share and d_weight rows are
+    buffers of their own, so a write past a shard's rows is caught."""
+    ensure_built()
+    w, gin = _inputs(CASES[ci], 70 + ci)
+    T, H, V, c, tau = w.T, w.H, w.V, w.chunk_size, w.temperature
+    cuts = sorted({0, V} | ({V // 3, (2 * V) // 3} if V >= 3 else set()))
+    shards = list(zip(cuts[:-1], cuts[1:]))
+    parts = []
+    for j, (a, b) in enumerate(shards):
+        wsh = Guarded((b - a, H), torch.bfloat16, 80 + j, gin["weight"].t[a:b])
+        ws = Guarded((lm.lmhead_workspace_size(0, T, H, b - a, c),), torch.uint8, 90 + j)
+        part = Guarded((T, 4), torch.float32, 100 + j)
+        rc = lm.lmhead_logps_fwd_shard(gin["hidden"].t, wsh.t, gin["targets"].t, _mask(gin), a,
+                                       V, tau, c, part.t, ws.t)
+        assert rc == 0 and lm.lmhead_read_device_status(ws.t) == 0
+        _check(dict(gin, weight_shard=wsh), {"partials": part, "workspace": ws},
+               "lmhead_logps_fwd_shard (shard %d)" % j)
+        parts.append(part)
+    allp = Guarded((len(shards), T, 4), torch.float32, 110,
+                   torch.stack([p_.t for p_ in parts]).cpu())
+    out = {n: Guarded((T,), torch.float32, 111 + i) for i, n in enumerate(("logp", "entropy", "lse"))}
+    rc = lm.lmhead_combine_shards(allp.t, gin["targets"].t, _mask(gin), V, out["logp"].t,
+                                  out["entropy"].t, out["lse"].t)
+    assert rc == 0
+    _check(dict(gin, partials=allp), out, "lmhead_combine_shards")
+    for b in out.values():
+        b.rearm()
+    for j, (a, b) in enumerate(shards):
+        wsh = Guarded((b - a, H), torch.bfloat16, 120 + j, gin["weight"].t[a:b])
+        ws = Guarded((lm.lmhead_workspace_size(1, T, H, b - a, c),), torch.uint8, 130 + j)
+        dh = Guarded((T, H), torch.float32, 140 + j)
+        dw = Guarded((b - a, H), torch.float32, 150 + j, torch.randn((b - a, H)))
+        rc = lm.lmhead_logps_bwd_shard(gin["hidden"].t, wsh.t, gin["targets"].t, _mask(gin), a,
+                                       V, tau, c, gin["grad_logp"].t, gin["grad_entropy"].t,
+                                       out["lse"].t, out["entropy"].t, dh.t, dw.t, j % 2, ws.t)
+        assert rc == 0 and lm.lmhead_read_device_status(ws.t) == 0
+        assert torch.isfinite(dh.t).all() and torch.isfinite(dw.t).all()
+        _check(dict(gin, weight_shard=wsh, lse=out["lse"], entropy=out["entropy"]),
+               {"d_hidden": dh, "d_weight_shard": dw, "workspace": ws},
+               "lmhead_logps_bwd_shard (shard %d)" % j)
