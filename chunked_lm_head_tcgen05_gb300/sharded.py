@@ -177,3 +177,53 @@ def token_parallel_backward(hidden, weight, targets, loss_mask, temperature, chu
     if reduce:
         dist.all_reduce(d_weight, op=dist.ReduceOp.SUM, group=group)
     return d_hidden, d_weight
+
+
+class VocabParallelLogps(torch.autograd.Function):
+    """Autograd over the vocabulary-parallel head: (hidden [T,H], this rank's
+    weight_shard [rows, H], targets, loss_mask, vocab_offset, vocab_total,
+    temperature, chunk_size, group, ops, main_grad) -> (logp, entropy) over the
+    whole vocabulary.  hidden's gradient is summed over ranks (all-reduce), the
+    shard's gradient stays on this rank; with main_grad (fp32 [rows, H]) it is
+    added there in fp32 instead of being returned."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
+                temperature, chunk_size, group, ops, main_grad):
+        logp, ent, lse = vocab_parallel_forward(hidden, weight_shard, targets, loss_mask,
+                                                vocab_offset, vocab_total, temperature,
+                                                chunk_size, group=group, ops=ops)
+        ctx.save_for_backward(hidden, weight_shard, targets, loss_mask, lse, ent)
+        ctx.args = (vocab_offset, vocab_total, temperature, chunk_size, group, ops, main_grad)
+        ctx.set_materialize_grads(False)
+        return logp, ent
+
+    @staticmethod
+    def backward(ctx, g_logp, g_ent):
+        hidden, weight_shard, targets, loss_mask, lse, ent = ctx.saved_tensors
+        vocab_offset, vocab_total, temperature, chunk_size, group, ops, main_grad = ctx.args
+        none = (None,) * 11
+        need_h, need_w = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if (g_logp is None and g_ent is None) or not (need_h or need_w):
+            return none
+        dt = lse.dtype
+        gl = None if g_logp is None else g_logp.to(dt).contiguous()
+        ge = None if g_ent is None else g_ent.to(dt).contiguous()
+        main = main_grad if need_w else None
+        d_hidden, d_w = vocab_parallel_backward(
+            hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total, temperature,
+            chunk_size, gl, ge, lse, ent, d_weight_shard=main, accumulate=main is not None,
+            group=group, ops=ops)
+        return ((d_hidden if need_h else None, d_w if (need_w and main is None) else None)
+                + (None,) * 9)
+
+
+def vocab_parallel_logps(hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
+                         temperature=1.0, chunk_size=512, group=None, ops=None, main_grad=None):
+    """(logp, entropy) over the whole vocabulary, differentiable in hidden and in
+    this rank's weight_shard (main_grad: see VocabParallelLogps)."""
+    if main_grad is None:
+        main_grad = getattr(weight_shard, "main_grad", None)
+    return VocabParallelLogps.apply(hidden, weight_shard, targets, loss_mask, int(vocab_offset),
+                                    int(vocab_total), float(temperature), int(chunk_size), group,
+                                    ops, main_grad)

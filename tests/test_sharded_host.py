@@ -62,10 +62,11 @@ class NumpyShardOps:
         s1 = (wgt * (p[:, :, 2] + (p[:, :, 0] - M) * p[:, :, 1])).sum(axis=0)
         zy = p[:, :, 3].max(axis=0)
         valid, _ = self._local(targets, 0, Vt, Vt)
-        l2s = np.log2(s)
+        with np.errstate(divide="ignore", invalid="ignore"):   # unscored rows: zeros, reset below
+            l2s = np.log2(s)
+            ent = (l2s - s1 / s) / LOG2E
         lse = (M + l2s) / LOG2E
         logp = np.where(valid, (zy - M - l2s) / LOG2E, np.nan)
-        ent = (l2s - s1 / s) / LOG2E
         if loss_mask is not None:
             off = loss_mask.numpy() == 0
             lse[off], logp[off], ent[off] = 0.0, 0.0, 0.0
@@ -173,6 +174,44 @@ def _rank(rank, world, port, kind):
             assert dw is dwt
     finally:
         dist.destroy_process_group()
+
+
+def _rank_autograd(rank, world, port, use_main):
+    """The vocabulary-parallel autograd function: a loss over logp and entropy,
+    differentiated through the exchanges, against the oracle."""
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from chunked_lm_head_tcgen05_gb300 import sharded
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w, x = _inputs()
+        _, _, _, o_dh, o_dw = _oracle(x, w)
+        v0, rows = sharded.shard_range(w.V, rank, world)
+        # fp64 copies of the bf16 values, so the gradients come back unrounded
+        h = x["hidden"].double().requires_grad_(True)
+        ws = x["weight"][v0:v0 + rows].double().requires_grad_(True)
+        main = torch.zeros((rows, w.H), dtype=torch.float64) if use_main else None
+        logp, ent = sharded.vocab_parallel_logps(h, ws, x["targets"], x["loss_mask"], v0, w.V,
+                                                 w.temperature, w.chunk_size, ops=NumpyShardOps(),
+                                                 main_grad=main)
+        loss = (x["grad_logp"].double() * logp).sum() + (x["grad_entropy"].double() * ent).sum()
+        loss.backward()
+        np.testing.assert_allclose(h.grad.numpy(), o_dh, rtol=0, atol=1e-12)
+        got = main.numpy() if use_main else ws.grad.numpy()
+        if use_main:
+            assert ws.grad is None
+        # the shard's gradient buffer is fp32, as the library's d_weight is
+        np.testing.assert_allclose(got, o_dw[v0:v0 + rows], rtol=1e-6, atol=1e-12)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("use_main", [False, True])
+def test_two_gloo_ranks_vocab_parallel_autograd(use_main):
+    mp.start_processes(_rank_autograd, args=(2, _free_port(), use_main), nprocs=2, join=True,
+                       start_method="spawn")
 
 
 @pytest.mark.parametrize("kind", ["vocab", "token"])
