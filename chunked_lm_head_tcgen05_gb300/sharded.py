@@ -185,7 +185,9 @@ class VocabParallelLogps(torch.autograd.Function):
     temperature, chunk_size, group, ops, main_grad) -> (logp, entropy) over the
     whole vocabulary.  hidden's gradient is summed over ranks (all-reduce), the
     shard's gradient stays on this rank; with main_grad (fp32 [rows, H]) it is
-    added there in fp32 instead of being returned."""
+    added there in fp32 instead of being returned.  As with any collective, every
+    rank of the group runs the forward and the backward (the same inputs
+    requiring gradients on every rank)."""
 
     @staticmethod
     def forward(ctx, hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
