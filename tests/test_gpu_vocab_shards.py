@@ -141,3 +141,39 @@ def test_shards_full_vocabulary_qwen3_4b_size():
         assert np.abs(got[k] - ref[k]).max() <= 2e-5, k
     assert rel_fro(got["d_hidden"], ref["d_hidden"]) <= 1e-3
     assert rel_fro(got["d_weight"], ref["d_weight"]) <= 1e-3
+
+
+def _random_layout(i):
+    r = np.random.default_rng(20261202 + 5000 + i)
+    T = int(r.choice([1, 7, 129, 256, 257, int(r.integers(300, 700))]))
+    H = int(64 * r.integers(1, 6))
+    V = int(r.integers(2, 4000))
+    n = int(min(V, r.integers(1, 6)))
+    cuts = sorted(int(c) for c in r.choice(np.arange(1, V), size=n - 1, replace=False)) if n > 1 else []
+    bounds = [0] + cuts + [V]
+    mask = str(r.choice(["none", "bernoulli", "prompt_prefix"]))
+    extra = {"mask_drop": float(r.uniform(0.05, 0.8))} if mask == "bernoulli" else (
+        {"rows": 1} if mask == "prompt_prefix" else {})
+    w = W.WORKLOADS["tiny"].with_(T=T, H=H, V=V, chunk_size=int(r.choice([1, 16, 64, 512])),
+                                  temperature=float(r.choice([0.5, 0.7, 1.0, 2.0])), mask=mask,
+                                  hidden_dist="rms", weight_std=float(r.choice([0.02, 0.05, 0.2])),
+                                  seed=int(r.integers(1, 1 << 30)), **extra)
+    return w, bounds, bool(r.random() > 0.3)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_shard_layouts(i):
+    """Seeded random shapes with 1-5 shards at random cut points."""
+    w, bounds, with_entropy = _random_layout(i)
+    x = W.make_inputs(w)
+    got = run_sharded(x, bounds, grad_entropy=with_entropy)
+    assert got["status"] == [0] * (2 * (len(bounds) - 1))
+    assert_parity(got, run_oracle(x, grad_entropy=with_entropy))
+    ref = run_gpu(x, grad_entropy=with_entropy)
+    for k in ("logp", "entropy", "lse"):
+        # fp32 summation order differs: a few ulps of the value's own magnitude
+        fin = np.isfinite(ref[k])
+        tol = 2e-5 * np.maximum(1.0, np.abs(ref[k][fin]))
+        assert np.all(np.abs(got[k][fin] - ref[k][fin]) <= tol), (k, bounds)
+    print(i, dict(T=w.T, H=w.H, V=w.V, chunk=w.chunk_size, tau=w.temperature, mask=w.mask),
+          bounds)
