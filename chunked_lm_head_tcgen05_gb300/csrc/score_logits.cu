@@ -2,8 +2,11 @@
 // per-row log-sum-exp, target log-prob and entropy (forward), and the
 // cotangent of the logits (backward), with the non-finite semantics stated
 // in include/lmhead.h.  Both passes are HBM-bound: one read of the logits
-// forward; one read and one write backward.  One CTA per row, 16-byte loads
-// when the row layout allows them.
+// forward; one read and one write backward.  The forward reduces a row in one
+// CTA; the backward, whose elements need only per-row values, spreads each
+// row over several CTAs (independent column ranges) so that the last wave of
+// rows does not leave most SMs idle.  16-byte loads when the row layout allows
+// them.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -14,8 +17,11 @@
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kUnroll = 4;   // 16-byte loads in flight per thread
+constexpr int kFwdThreads = 512;    // forward: one CTA per row
+constexpr int kThreads = 256;       // backward: one CTA per (row, column range)
+constexpr int kUnroll = 4;          // 16-byte loads in flight per thread
+constexpr int kMaxRowParts = 16;    // column ranges per row in the backward
+constexpr int kColsPerPart = 16384; // about 64 KB of fp32 logits per range
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -80,11 +86,12 @@ __device__ __forceinline__ Stats stats_merge(Stats a, Stats b) {
   return r;
 }
 
-__global__ void __launch_bounds__(kThreads)
+// One CTA per row (rows taken in turn when there are more rows than CTAs).
+__global__ void __launch_bounds__(kFwdThreads)
     score_logits_fwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ targets,
                             const uint8_t* __restrict__ mask, int64_t T, int V, float scale,
                             int vec4, float* logp, float* entropy, float* lse) {
-  __shared__ Stats red[kThreads / 32];
+  __shared__ Stats red[kFwdThreads / 32];
   __shared__ float zy_s;
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     if (mask && !mask[t]) {
@@ -102,11 +109,11 @@ __global__ void __launch_bounds__(kThreads)
       const float4* r4 = reinterpret_cast<const float4*>(row);
       const int n4 = V / 4;
       int i = threadIdx.x;
-      for (; i + (kUnroll - 1) * kThreads < n4; i += kUnroll * kThreads) {
+      for (; i + (kUnroll - 1) * kFwdThreads < n4; i += kUnroll * kFwdThreads) {
         float x[4 * kUnroll];
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {
-          const float4 q = r4[i + k * kThreads];
+          const float4 q = r4[i + k * kFwdThreads];
           x[4 * k] = q.x;
           x[4 * k + 1] = q.y;
           x[4 * k + 2] = q.z;
@@ -114,13 +121,13 @@ __global__ void __launch_bounds__(kThreads)
         }
         stats_add_chunk(st, x, scale);
       }
-      for (; i < n4; i += kThreads) {
+      for (; i < n4; i += kFwdThreads) {
         const float4 q = r4[i];
         const float x[4] = {q.x, q.y, q.z, q.w};
         stats_add_chunk(st, x, scale);
       }
     } else {
-      for (int i = threadIdx.x; i < V; i += kThreads) {
+      for (int i = threadIdx.x; i < V; i += kFwdThreads) {
         const float x[1] = {row[i]};
         stats_add_chunk(st, x, scale);
       }
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     if (threadIdx.x == 0) {
       Stats a = red[0];
-      for (int w = 1; w < kThreads / 32; ++w) a = stats_merge(a, red[w]);
+      for (int w = 1; w < kFwdThreads / 32; ++w) a = stats_merge(a, red[w]);
       float L, H, lp;
       if (a.bad) {
         L = H = lp = __int_as_float(0x7fc00000);
@@ -170,40 +177,48 @@ __device__ __forceinline__ float cotangent(float x, float scale, float lse_u, fl
   return g;
 }
 
+// Independent CTAs over (row, column range): kp ranges per row, work item w is
+// row w / kp, range w % kp.  Every element is read and written by one thread,
+// so d_logits may be the logits buffer itself.
 __global__ void __launch_bounds__(kThreads)
     score_logits_bwd_kernel(const float* logits, const int32_t* __restrict__ targets,
-                            const uint8_t* __restrict__ mask, int64_t T, int V, float scale,
-                            float inv_tau, int vec4, const float* __restrict__ grad_logp,
+                            const uint8_t* __restrict__ mask, int64_t T, int V, int kp,
+                            float scale, float inv_tau, int vec4,
+                            const float* __restrict__ grad_logp,
                             const float* __restrict__ grad_entropy,
                             const float* __restrict__ lse, const float* __restrict__ entropy,
                             float* d_logits) {
-  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+  const int n = vec4 ? V / 4 : V;
+  for (int64_t w = blockIdx.x; w < T * kp; w += gridDim.x) {
+    const int64_t t = w / kp;
+    const int part = static_cast<int>(w - t * kp);
+    const int b = static_cast<int>(static_cast<int64_t>(n) * part / kp);
+    const int e = static_cast<int>(static_cast<int64_t>(n) * (part + 1) / kp);
     const float* row = logits + t * static_cast<int64_t>(V);
     float* out = d_logits + t * static_cast<int64_t>(V);
     const bool scored = !mask || mask[t];
-    const float gl = scored && grad_logp ? grad_logp[t] : 0.f;
-    const float ge = scored && grad_entropy ? grad_entropy[t] : 0.f;
-    const float Hh = (grad_entropy && scored) ? entropy[t] : 0.f;
-    const float lse_u = scored ? lse[t] * kLog2e : 0.f;
-    const float a = ge * kLn2 * inv_tau;
-    const float b = fmaf(ge, Hh, gl) * inv_tau;
-    const float c1 = gl * inv_tau;
-    const int y = scored ? wrap_target(targets[t], V) : -1;
     if (!scored) {
       if (vec4) {
         float4* o4 = reinterpret_cast<float4*>(out);
-        for (int i = threadIdx.x; i < V / 4; i += kThreads) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = b + threadIdx.x; i < e; i += kThreads) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       } else {
-        for (int i = threadIdx.x; i < V; i += kThreads) out[i] = 0.f;
+        for (int i = b + threadIdx.x; i < e; i += kThreads) out[i] = 0.f;
       }
       continue;
     }
+    const float gl = grad_logp ? grad_logp[t] : 0.f;
+    const float ge = grad_entropy ? grad_entropy[t] : 0.f;
+    const float Hh = grad_entropy ? entropy[t] : 0.f;
+    const float lse_u = lse[t] * kLog2e;
+    const float a = ge * kLn2 * inv_tau;
+    const float bb = fmaf(ge, Hh, gl) * inv_tau;
+    const float c1 = gl * inv_tau;
+    const int y = wrap_target(targets[t], V);
     if (vec4) {
       const float4* r4 = reinterpret_cast<const float4*>(row);
       float4* o4 = reinterpret_cast<float4*>(out);
-      const int n4 = V / 4;
-      int i = threadIdx.x;
-      for (; i + (kUnroll - 1) * kThreads < n4; i += kUnroll * kThreads) {
+      int i = b + threadIdx.x;
+      for (; i + (kUnroll - 1) * kThreads < e; i += kUnroll * kThreads) {
         float4 q[kUnroll];
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) q[k] = r4[i + k * kThreads];
@@ -211,37 +226,43 @@ __global__ void __launch_bounds__(kThreads)
         for (int k = 0; k < kUnroll; ++k) {
           const int c = 4 * (i + k * kThreads);
           float4 g;
-          g.x = cotangent(q[k].x, scale, lse_u, a, b, c1, c == y);
-          g.y = cotangent(q[k].y, scale, lse_u, a, b, c1, c + 1 == y);
-          g.z = cotangent(q[k].z, scale, lse_u, a, b, c1, c + 2 == y);
-          g.w = cotangent(q[k].w, scale, lse_u, a, b, c1, c + 3 == y);
+          g.x = cotangent(q[k].x, scale, lse_u, a, bb, c1, c == y);
+          g.y = cotangent(q[k].y, scale, lse_u, a, bb, c1, c + 1 == y);
+          g.z = cotangent(q[k].z, scale, lse_u, a, bb, c1, c + 2 == y);
+          g.w = cotangent(q[k].w, scale, lse_u, a, bb, c1, c + 3 == y);
           o4[i + k * kThreads] = g;
         }
       }
-      for (; i < n4; i += kThreads) {
+      for (; i < e; i += kThreads) {
         const float4 q = r4[i];
         const int c = 4 * i;
         float4 g;
-        g.x = cotangent(q.x, scale, lse_u, a, b, c1, c == y);
-        g.y = cotangent(q.y, scale, lse_u, a, b, c1, c + 1 == y);
-        g.z = cotangent(q.z, scale, lse_u, a, b, c1, c + 2 == y);
-        g.w = cotangent(q.w, scale, lse_u, a, b, c1, c + 3 == y);
+        g.x = cotangent(q.x, scale, lse_u, a, bb, c1, c == y);
+        g.y = cotangent(q.y, scale, lse_u, a, bb, c1, c + 1 == y);
+        g.z = cotangent(q.z, scale, lse_u, a, bb, c1, c + 2 == y);
+        g.w = cotangent(q.w, scale, lse_u, a, bb, c1, c + 3 == y);
         o4[i] = g;
       }
     } else {
-      for (int i = threadIdx.x; i < V; i += kThreads)
-        out[i] = cotangent(row[i], scale, lse_u, a, b, c1, i == y);
+      for (int i = b + threadIdx.x; i < e; i += kThreads)
+        out[i] = cotangent(row[i], scale, lse_u, a, bb, c1, i == y);
     }
   }
 }
 
-int grid_rows(int64_t T) {
+int sm_count_now() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 152;
-  const int64_t cap = static_cast<int64_t>(sms) * 4;
-  return static_cast<int>(T < cap ? T : cap);
+  return sms;
+}
+
+// Column ranges per row in the backward: about kColsPerPart columns each, at
+// most `cap`.
+int parts_per_row(int V, int cap) {
+  const int k = V / kColsPerPart;
+  return k < 1 ? 1 : (k > cap ? cap : k);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -254,8 +275,10 @@ cudaError_t launch_score_logits_fwd(const float* logits, const int32_t* targets,
                                     const uint8_t* mask, int64_t T, int V, float tau, float* logp,
                                     float* entropy, float* lse, cudaStream_t s) {
   const int vec4 = (V % 4 == 0 && aligned16(logits)) ? 1 : 0;
-  score_logits_fwd_kernel<<<grid_rows(T), kThreads, 0, s>>>(logits, targets, mask, T, V,
-                                                             kLog2e / tau, vec4, logp, entropy, lse);
+  const int64_t cap = static_cast<int64_t>(sm_count_now()) * 4;
+  const int grid = static_cast<int>(T < cap ? T : cap);
+  score_logits_fwd_kernel<<<grid, kFwdThreads, 0, s>>>(logits, targets, mask, T, V,
+                                                        kLog2e / tau, vec4, logp, entropy, lse);
   return cudaGetLastError();
 }
 
@@ -265,9 +288,13 @@ cudaError_t launch_score_logits_bwd(const float* logits, const int32_t* targets,
                                     const float* lse, const float* entropy, float* d_logits,
                                     cudaStream_t s) {
   const int vec4 = (V % 4 == 0 && aligned16(logits) && aligned16(d_logits)) ? 1 : 0;
-  score_logits_bwd_kernel<<<grid_rows(T), kThreads, 0, s>>>(
-      logits, targets, mask, T, V, kLog2e / tau, 1.0f / tau, vec4, grad_logp, grad_entropy, lse,
-      entropy, d_logits);
+  const int kp = parts_per_row(V, kMaxRowParts);
+  const int64_t cap = static_cast<int64_t>(sm_count_now()) * 16;
+  const int64_t items = T * kp;
+  const int grid = static_cast<int>(items < cap ? items : cap);
+  score_logits_bwd_kernel<<<grid, kThreads, 0, s>>>(logits, targets, mask, T, V, kp,
+                                                     kLog2e / tau, 1.0f / tau, vec4, grad_logp,
+                                                     grad_entropy, lse, entropy, d_logits);
   return cudaGetLastError();
 }
 

@@ -166,7 +166,7 @@ def test_noalloc_forward_stays_in_bounds():
     _check(gin, out, "lmhead_logps_fwd_noalloc")
 
 
-@pytest.mark.parametrize("V", [3001, 3000])
+@pytest.mark.parametrize("V", [3001, 3000, 40001, 40000])
 def test_score_logits_stays_in_bounds(V):
     ensure_built()
     T, tau = 133, 0.9

@@ -37,7 +37,9 @@ def _same_pattern(a, b):
         and np.array_equal(np.isneginf(a), np.isneginf(b))
 
 
-@pytest.mark.parametrize("V", [3001, 3000])
+# 3000 / 3001: one CTA per row; 70000 / 70001: rows spread over a cluster of 4 CTAs in
+# the forward and 4 independent CTAs in the backward (16-byte and scalar load paths)
+@pytest.mark.parametrize("V", [3001, 3000, 70001, 70000])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_score_logits_against_oracle(V, in_place):
     ensure_built()
