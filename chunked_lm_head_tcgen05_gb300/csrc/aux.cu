@@ -328,10 +328,37 @@ __global__ void zero_masked_rows_kernel(const uint8_t* __restrict__ mask, int T,
 // d = u - lse_u = log2 p:  dz / tau = -p (a d + b) + c1 [c == y]  (the
 // per-row coefficients of bwd_prep_kernel), written back as bf16.  Rows
 // past the scored count have zero coefficients and become exact zeros.
+// Work items are (row, column range) pairs, `parts` ranges of 8-element
+// groups per row, so that the CTAs share the pass evenly (with whole rows per
+// CTA, 3,840 rows on 1,216 CTAs left the fourth round on a sixth of them).
+// Every element is read and written by one thread.  By count, the one ex2
+// per logit occupies the special-function units for about 40% of the pass,
+// and four loads in flight per thread (fewer resident warps) measured slower.
+__device__ __forceinline__ uint4 dz_group(uint4 raw, int c0, float base, float4 cf, int y) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+    float g[2];
+    const float uu[2] = {u.x, u.y};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float d = uu[e] + base;
+      const float pr = ex2_approx(d);
+      g[e] = -pr * fmaf(cf.y, d, cf.z);
+      if (c0 + 2 * k + e == y) g[e] += cf.w;
+    }
+    const __nv_bfloat162 bv = __floats2bfloat162_rn(g[0], g[1]);
+    out[k] = *reinterpret_cast<const uint32_t*>(&bv);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 __global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* __restrict__ m_tile,
                                 int mt_ld, const float4* __restrict__ coef,
                                 const int* __restrict__ y_c, const DeviceState* st, int t0,
-                                int rows_cap, int V) {
+                                int rows_cap, int V, int parts) {
   pdl_wait_prerequisites();
   pdl_launch_dependents();
   int dyn = st->rows - t0;
@@ -339,40 +366,27 @@ __global__ void fused_dz_kernel(uint16_t* __restrict__ z, int ld, const float* _
   // rows the gradient GEMMs read: whole 128-row tiles (zero padding rows included)
   const int rows = min(rows_cap, (dyn + BM - 1) / BM * BM);
   const int groups = (V + 7) / 8;
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+  for (int64_t w = blockIdx.x; w < static_cast<int64_t>(rows) * parts; w += gridDim.x) {
+    const int r = static_cast<int>(w / parts);
+    const int part = static_cast<int>(w - static_cast<int64_t>(r) * parts);
+    const int g0 = static_cast<int>(static_cast<int64_t>(groups) * part / parts);
+    const int g1 = static_cast<int>(static_cast<int64_t>(groups) * (part + 1) / parts);
     const float4 cf = coef[t0 + r];
     const int y = y_c[t0 + r];
     const float* mt = m_tile + static_cast<int64_t>(r) * mt_ld;
     uint16_t* zr = z + static_cast<int64_t>(r) * ld;
-    for (int gi = threadIdx.x; gi < groups; gi += blockDim.x) {
+    for (int gi = g0 + threadIdx.x; gi < g1; gi += blockDim.x) {
       const int c0 = gi * 8;
-      const float base = mt[c0 / BN] - cf.x;
       uint16_t* row = zr + c0;
-      const uint4 raw = *reinterpret_cast<const uint4*>(row);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t out[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-        float g[2];
-        const float uu[2] = {u.x, u.y};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float d = uu[e] + base;
-          const float pr = ex2_approx(d);
-          g[e] = -pr * fmaf(cf.y, d, cf.z);
-          if (c0 + 2 * k + e == y) g[e] += cf.w;
-        }
-        const __nv_bfloat162 b = __floats2bfloat162_rn(g[0], g[1]);
-        out[k] = *reinterpret_cast<const uint32_t*>(&b);
-      }
+      const uint4 o = dz_group(*reinterpret_cast<const uint4*>(row), c0, mt[c0 / BN] - cf.x, cf, y);
       if (c0 + 8 <= V) {
-        *reinterpret_cast<uint4*>(row) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(row) = o;
       } else {
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (c0 + j < V)
-            row[j] = static_cast<uint16_t>((j & 1) ? (out[j >> 1] >> 16) : (out[j >> 1] & 0xFFFFu));
+            row[j] = static_cast<uint16_t>((j & 1) ? (ow[j >> 1] >> 16) : (ow[j >> 1] & 0xFFFFu));
       }
     }
   }
@@ -480,8 +494,11 @@ cudaError_t launch_bwd_prep(const int* idx, const DeviceState* st, int r0, int r
 cudaError_t launch_fused_dz(uint16_t* z16, int ld, const float* m_tile, int m_tile_ld,
                             const float4* coef, const int* y_c, const DeviceState* st, int t0,
                             int rows_cap, int V, cudaStream_t s) {
-  return launch_pdl(fused_dz_kernel, grid_for(rows_cap, 1, 152 * 8), 256, s, z16, ld, m_tile,
-                    m_tile_ld, coef, y_c, st, t0, rows_cap, V);
+  // ranges of about 4096 groups (32,768 logits, 64 KB read and written) per row
+  const int groups = (V + 7) / 8;
+  const int parts = (groups + 4095) / 4096;
+  return launch_pdl(fused_dz_kernel, grid_for(static_cast<int64_t>(rows_cap) * parts, 1, 152 * 8),
+                    256, s, z16, ld, m_tile, m_tile_ld, coef, y_c, st, t0, rows_cap, V, parts);
 }
 
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int T, int H, float* d_hidden,
