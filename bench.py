@@ -672,13 +672,13 @@ def measure_workload(lm, name, args, world, dev, stream, clocks, timer, cpu=True
         t, i = timer(hd.step, k, name + ":fwd_bwd")
         ts.append(t / k)
         mhz.append(clocks.region_mhz(i))
-    ms = median(ts)
+    step_s = median(ts)
     res = {"config": workload_label(w, Tv), "steps_per_region": k, "regions": reps,
-           "ms_per_step": ms * 1e3, "ms_per_step_all": [t * 1e3 for t in ts],
-           "tokens_per_s": Tv * world / ms,
-           "tflops_counted": 6.0 * Tv * H * V / ms / 1e12,
-           "tflops_executed": 8.0 * Tv * H * V / ms / 1e12}
-    peak, kind, _ = bf16_peak(k * ms)
+           "ms_per_step": step_s * 1e3, "ms_per_step_all": [t * 1e3 for t in ts],
+           "tokens_per_s": Tv * world / step_s,
+           "tflops_counted": 6.0 * Tv * H * V / step_s / 1e12,
+           "tflops_executed": 8.0 * Tv * H * V / step_s / 1e12}
+    peak, kind, _ = bf16_peak(k * step_s)
     res["frac_peak_counted"] = res["tflops_counted"] / peak
     res["peak_kind"] = kind
     cl = clocks.summary({name + ":fwd_bwd"})
@@ -695,7 +695,7 @@ def measure_workload(lm, name, args, world, dev, stream, clocks, timer, cpu=True
     res["fwd"] = {"ms": f * 1e3, "tokens_per_s": Tv * world / f,
                   "tflops": 2.0 * Tv * H * V / f / 1e12}
     # dominant kernel of the fwd + bwd step
-    nk = max(3, k // 2, min(400, int(math.ceil(SUSTAINED_REGION_S / max(ms, 1e-6)))))
+    nk = max(3, k // 2, min(400, int(math.ceil(SUSTAINED_REGION_S / max(step_s, 1e-6)))))
     per, treg = kernel_profile(lm, timer, hd.step, nk, name + ":profile")
     res["roofline"] = roofline_of(per, nk, Tv, H, V, treg, name)
     res["kernels"] = kernel_shares(per, nk)
@@ -711,7 +711,7 @@ def measure_workload(lm, name, args, world, dev, stream, clocks, timer, cpu=True
         res["single_call_fwd_bwd"] = {"strategy": "keep_logits", "block_tokens": tb,
                                       "ms_per_step": s * 1e3, "tokens_per_s": Tv * world / s,
                                       "tflops_counted": 6.0 * Tv * H * V / s / 1e12,
-                                      "speedup_vs_two_calls": ms / s}
+                                      "speedup_vs_two_calls": step_s / s}
         hd.step()   # leave the two-call results for the parity check below
     else:
         res["single_call_fwd_bwd"] = {"strategy": "recompute (the two calls above)"}
