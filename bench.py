@@ -655,7 +655,6 @@ def measure_workload(lm, name, args, world, dev, stream, clocks, timer, cpu=True
     alone, the single-call path where its cost model keeps the logits, the
     dominant kernel, the clock record and the oracle timed beside it."""
     import torch
-    from chunked_lm_head_tcgen05_gb300 import workloads
     t_gen = time.perf_counter()
     w, x = workload_inputs(name)
     t_gen = time.perf_counter() - t_gen
