@@ -17,7 +17,8 @@
 
 namespace {
 
-constexpr int kFwdThreads = 512;    // forward: one CTA per row
+constexpr int kFwdThreads = 256;    // forward: one CTA per row
+constexpr int kFwdUnroll = 8;       // forward: 16-byte loads in flight per thread
 constexpr int kThreads = 256;       // backward: one CTA per (row, column range)
 constexpr int kUnroll = 4;          // 16-byte loads in flight per thread
 constexpr int kMaxRowParts = 16;    // column ranges per row in the backward
@@ -109,10 +110,10 @@ __global__ void __launch_bounds__(kFwdThreads)
       const float4* r4 = reinterpret_cast<const float4*>(row);
       const int n4 = V / 4;
       int i = threadIdx.x;
-      for (; i + (kUnroll - 1) * kFwdThreads < n4; i += kUnroll * kFwdThreads) {
-        float x[4 * kUnroll];
+      for (; i + (kFwdUnroll - 1) * kFwdThreads < n4; i += kFwdUnroll * kFwdThreads) {
+        float x[4 * kFwdUnroll];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
+        for (int k = 0; k < kFwdUnroll; ++k) {
           const float4 q = r4[i + k * kFwdThreads];
           x[4 * k] = q.x;
           x[4 * k + 1] = q.y;
