@@ -27,9 +27,9 @@ backend after the library's work on the current stream.
 import torch
 import torch.distributed as dist
 
-from . import (LMHEAD_OP_BWD, LMHEAD_OP_FWD, LmheadError, lmhead_combine_shards,
-               lmhead_logps_bwd, lmhead_logps_bwd_shard, lmhead_logps_fwd,
-               lmhead_logps_fwd_shard, lmhead_workspace_size)
+from . import (LmheadError, lmhead_combine_shards, lmhead_logps_bwd, lmhead_logps_bwd_shard,
+               lmhead_logps_fwd, lmhead_logps_fwd_shard)
+from .autograd import _workspace
 
 
 def shard_range(vocab_total, rank, world):
@@ -41,23 +41,21 @@ def shard_range(vocab_total, rank, world):
 
 
 class LibraryOps:
-    """The per-rank calls, run by the library on the tensors' GPU."""
+    """The per-rank calls, run by the library on the tensors' GPU.  Workspaces
+    come from one buffer per (device, stream), reused across calls (the
+    autograd wrapper's cache), unless the caller passes its own."""
 
     @staticmethod
-    def _ws(op, T, H, V, chunk_size, device, workspace):
-        need = lmhead_workspace_size(op, T, H, V, chunk_size)
-        if need == 0:
-            raise LmheadError(1, "lmhead_workspace_size")
-        if workspace is not None and workspace.numel() * workspace.element_size() >= need:
+    def _ws(T, H, V, chunk_size, device, workspace):
+        if workspace is not None:
             return workspace
-        return torch.empty(need, dtype=torch.uint8, device=device)
+        return _workspace(T, H, V, chunk_size, device)
 
     def shard_forward(self, hidden, weight_shard, targets, loss_mask, vocab_offset, vocab_total,
                       temperature, chunk_size, workspace=None):
         T, H = hidden.shape
         part = torch.empty((T, 4), dtype=torch.float32, device=hidden.device)
-        ws = self._ws(LMHEAD_OP_FWD, T, H, weight_shard.shape[0], chunk_size, hidden.device,
-                      workspace)
+        ws = self._ws(T, H, weight_shard.shape[0], chunk_size, hidden.device, workspace)
         rc = lmhead_logps_fwd_shard(hidden, weight_shard, targets, loss_mask, vocab_offset,
                                     vocab_total, temperature, chunk_size, part, ws)
         if rc:
@@ -78,8 +76,7 @@ class LibraryOps:
                        d_weight_shard, accumulate, workspace=None):
         T, H = hidden.shape
         d_hidden = torch.empty((T, H), dtype=torch.float32, device=hidden.device)
-        ws = self._ws(LMHEAD_OP_BWD, T, H, weight_shard.shape[0], chunk_size, hidden.device,
-                      workspace)
+        ws = self._ws(T, H, weight_shard.shape[0], chunk_size, hidden.device, workspace)
         rc = lmhead_logps_bwd_shard(hidden, weight_shard, targets, loss_mask, vocab_offset,
                                     vocab_total, temperature, chunk_size, grad_logp, grad_entropy,
                                     lse, entropy if grad_entropy is not None else None, d_hidden,
@@ -93,7 +90,7 @@ class LibraryOps:
         T, H = hidden.shape
         dev = hidden.device
         logp, ent, lse = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
-        ws = self._ws(LMHEAD_OP_FWD, T, H, weight.shape[0], chunk_size, dev, workspace)
+        ws = self._ws(T, H, weight.shape[0], chunk_size, dev, workspace)
         rc = lmhead_logps_fwd(hidden, weight, targets, loss_mask, temperature, chunk_size, logp,
                               ent, lse, ws)
         if rc:
@@ -105,7 +102,7 @@ class LibraryOps:
         T, H = hidden.shape
         dev = hidden.device
         d_hidden = torch.empty((T, H), dtype=torch.float32, device=dev)
-        ws = self._ws(LMHEAD_OP_BWD, T, H, weight.shape[0], chunk_size, dev, workspace)
+        ws = self._ws(T, H, weight.shape[0], chunk_size, dev, workspace)
         rc = lmhead_logps_bwd(hidden, weight, targets, loss_mask, temperature, chunk_size,
                               grad_logp, grad_entropy, lse,
                               entropy if grad_entropy is not None else None, d_hidden, d_weight,
