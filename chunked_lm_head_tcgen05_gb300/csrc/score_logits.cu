@@ -38,14 +38,22 @@ struct Stats {
 };
 
 // Fold n values into the running statistics: one max over the chunk, then
-// the exponentials against it.  NaN / +inf set `bad`; -inf is skipped.
+// the exponentials against it.  NaN or +inf set `bad` (NaN by its failed
+// self-comparison, +inf through the maximum); -inf adds exactly nothing: its
+// exponent d is clamped to -1e30, whose ex2 is +0, so e and e * d are zeros.
+// A NaN's exponent is clamped the same way; its row is reported as NaN anyway.
 template <int N>
 __device__ __forceinline__ void stats_add_chunk(Stats& st, const float (&x)[N], float scale) {
   float cmax = -INFINITY;
+  bool nan = false;
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    if (isnan(x[j]) || x[j] == INFINITY) st.bad = 1;
-    else cmax = fmaxf(cmax, x[j]);
+    cmax = fmaxf(cmax, x[j]);   // ignores NaN
+    nan |= x[j] != x[j];
+  }
+  if (nan || cmax == INFINITY) {
+    st.bad = 1;
+    return;   // the row's results are NaN: its sums are never used
   }
   const float cm = cmax * scale;
   if (cm > st.m) {
@@ -57,12 +65,10 @@ __device__ __forceinline__ void stats_add_chunk(Stats& st, const float (&x)[N], 
   }
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    if (x[j] > -INFINITY && x[j] < INFINITY) {
-      const float d = fmaf(x[j], scale, -st.m);
-      const float e = lmh::ex2_approx(d);
-      st.s += e;
-      st.s1 = fmaf(e, d, st.s1);
-    }
+    const float d = fmaxf(fmaf(x[j], scale, -st.m), -1e30f);
+    const float e = lmh::ex2_approx(d);
+    st.s += e;
+    st.s1 = fmaf(e, d, st.s1);
   }
 }
 
